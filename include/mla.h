@@ -1,0 +1,170 @@
+/*
+ * mla.h — C ABI of the GB300 (sm_103a) latent causal attention library.
+ *
+ * Two calls make up the path:
+ *
+ *   mla_kv_latent_project   latent = hidden @ w_down, then optionally
+ *                           k = latent @ w_up_k and v = latent @ w_up_v.
+ *                           Page "FW-GLM-5-1 l2_p1" (fused latent
+ *                           projection), its problem statement.
+ *
+ *   mla_latent_attention    causal multi-head attention whose keys and values
+ *                           are rebuilt per head from a per-position latent:
+ *                           for batch b, head h and query position t,
+ *                             k_s = kv_latent[b,s] @ w_up_k[:,h]
+ *                             v_s = kv_latent[b,s] @ w_up_v[:,h]
+ *                             out[b,t,h] = sum_{s<=t} softmax_s(scale * q[b,t,h].k_s) v_s
+ *                           Page "FW-GLM-5-1 l2_p31" (fused MLA-style attention
+ *                           from compressed KV latents), "The algorithm".
+ *
+ * Conventions for every call:
+ *   - Pointers named as tensors are DEVICE pointers (cudaMalloc'd or from a
+ *     framework allocator) to contiguous row-major data; the caller owns
+ *     every buffer.  The library never allocates, frees, copies to the host
+ *     or synchronises, and never writes its inputs.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
+ *     enqueued asynchronously on it.
+ *   - The return value reports host-side validation and launch errors only.
+ *     A kernel that fails later (for example a device-side wait that ran out
+ *     of time, see mla_get_device_error) shows up after the caller's next
+ *     synchronisation, as usual in CUDA.
+ *   - dtype codes: MLA_F32 (IEEE fp32), MLA_BF16 (bfloat16).  All
+ *     accumulation is fp32.  Supported (in, out) pairs: (F32, F32),
+ *     (BF16, F32), (BF16, BF16).
+ *   - No C++ exceptions cross this boundary.  Functions are thread-safe as
+ *     long as concurrent calls use distinct output and workspace buffers;
+ *     mla_set_option is the exception (process-global, not synchronised).
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_F32 = 0,
+  MLA_BF16 = 1
+} mla_dtype_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_NULL = 1,          /* a required pointer is NULL                     */
+  MLA_ERR_SHAPE = 2,         /* a size is non-positive, inconsistent or too big */
+  MLA_ERR_DTYPE = 3,         /* unsupported dtype or (in, out) combination     */
+  MLA_ERR_ALIGN = 4,         /* a pointer is not 16-byte aligned               */
+  MLA_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than required        */
+  MLA_ERR_CUDA = 6,          /* a CUDA runtime/driver call failed              */
+  MLA_ERR_TIMEOUT = 7,       /* a device-side wait ran out of time             */
+  MLA_ERR_UNSUPPORTED = 8    /* valid request this build has no kernel for     */
+} mla_status_t;
+
+/*
+ * latent = hidden @ w_down; k = latent @ w_up_k; v = latent @ w_up_v.
+ * (Page "FW-GLM-5-1 l2_p1", problem statement: hidden (B,T,model_dim) viewed
+ * as (M = B*T, model_dim), w_down (model_dim, rank), w_up_k / w_up_v
+ * (rank, kv_dim) with kv_dim = heads * head_dim.)
+ *
+ *   hidden  (M, model_dim)       in_dtype
+ *   w_down  (model_dim, rank)    in_dtype
+ *   w_up_k  (rank, kv_dim)       in_dtype   may be NULL together with k
+ *   w_up_v  (rank, kv_dim)       in_dtype   may be NULL together with v
+ *   latent  (M, rank)            out_dtype  written
+ *   k, v    (M, kv_dim)          out_dtype  written if non-NULL
+ * k and v are computed from the fp32 latent (before any rounding to out_dtype).
+ * bf16 inputs use the tensor-core path, which needs 16-byte aligned pointers,
+ * model_dim % 64 == 0, rank % 64 == 0 (rank <= 512) and kv_dim % 64 == 0;
+ * fp32 inputs take the CUDA-core path (any positive sizes, rank <= 256).
+ * Errors: MLA_ERR_NULL (hidden, w_down or latent NULL; k given without
+ * w_up_k; v without w_up_v), MLA_ERR_SHAPE, MLA_ERR_DTYPE, MLA_ERR_ALIGN,
+ * MLA_ERR_CUDA.
+ */
+mla_status_t mla_kv_latent_project(const void* hidden, const void* w_down, const void* w_up_k,
+                                   const void* w_up_v, void* latent, void* k, void* v,
+                                   int64_t M, int model_dim, int rank, int kv_dim,
+                                   int in_dtype, int out_dtype, void* stream);
+
+/*
+ * Device workspace, in bytes, that mla_latent_attention needs for these sizes
+ * (0 when the chosen path needs none).  Pure host function.
+ */
+size_t mla_latent_attention_workspace_size(int B, int Tq, int Tkv, int H, int d, int rank,
+                                           int in_dtype, int causal);
+
+/*
+ * out[b,i,h,:] = sum_s softmax_s(scale * q[b,i,h,:] . k_s) * v_s with
+ * k_s = kv_latent[b,s,:] @ w_up_k[:,h,:], v_s = kv_latent[b,s,:] @ w_up_v[:,h,:].
+ * (Page "FW-GLM-5-1 l2_p31", "The algorithm": mask s <= t inclusive.)
+ *
+ *   q          (B, Tq, H, d)      in_dtype
+ *   kv_latent  (B, Tkv, rank)     in_dtype
+ *   w_up_k     (rank, H, d)       in_dtype
+ *   w_up_v     (rank, H, d)       in_dtype
+ *   out        (B, Tq, H, d)      out_dtype   written
+ *   workspace  device scratch of at least
+ *              mla_latent_attention_workspace_size(...) bytes, 256-byte
+ *              aligned, owned by the caller, contents need not be initialised
+ *              (NULL allowed when that size is 0).
+ * Query i sits at position t = Tkv - Tq + i (the queries are the LAST Tq
+ * positions; Tq == Tkv is prefill, Tq == 1 is decoding the newest position).
+ * causal != 0 lets query t see keys s <= t; causal == 0 lets every query see
+ * all Tkv keys.  Requires 1 <= Tq <= Tkv.
+ *
+ * Paths (chosen from dtype and shape; same results within tolerance):
+ *   - bf16 with d % 64 == 0, rank % 64 == 0, rank <= 512, d <= 256 and
+ *     16-byte aligned pointers: tensor-core path (query absorbed into the
+ *     latent space, flash loop over TMA-staged latent tiles with tcgen05).
+ *   - otherwise (fp32, or small/odd shapes): warp-per-query CUDA-core path
+ *     (rank <= 1024, d <= 256).
+ * Errors: MLA_ERR_NULL, MLA_ERR_SHAPE, MLA_ERR_DTYPE, MLA_ERR_ALIGN,
+ * MLA_ERR_WORKSPACE, MLA_ERR_CUDA.
+ */
+mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const void* w_up_k,
+                                  const void* w_up_v, void* out, int B, int Tq, int Tkv, int H,
+                                  int d, int rank, float scale, int causal, int in_dtype,
+                                  int out_dtype, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
+ * Split-KV merge (the online-softmax merge of partial states; page
+ * "Kimi-K2.6 l2_p29", online softmax with running max and rescaling by
+ * exp(m - m_new), -inf handling): for each row r and part p < parts,
+ *   m[p,r]  running max of part p, in log2 units (scores already multiplied
+ *           by log2(e)); -inf marks an empty part,
+ *   l[p,r]  sum of 2^(score - m[p,r]) over the part,
+ *   o[p,r,:] (width floats) sum of 2^(score - m[p,r]) * value over the part;
+ *   out[r,:] = sum_p 2^(m[p,r]-M) o[p,r,:] / sum_p 2^(m[p,r]-M) l[p,r],
+ *   M = max_p m[p,r].  A row whose parts are all empty gets 0.
+ * All fp32 device pointers; out is (rows, width) in out_dtype.
+ * This is the step the attention call runs between its split-KV partitions.
+ */
+mla_status_t mla_merge_partials(const float* m, const float* l, const float* o, void* out,
+                                int parts, int rows, int width, int out_dtype, void* stream);
+
+/*
+ * Device-side error word (0 = none).  A kernel whose internal wait runs past
+ * its limit (2 s) records MLA_ERR_TIMEOUT's cause there and exits early
+ * instead of hanging.  Synchronises the device.  clear != 0 resets it.
+ */
+mla_status_t mla_get_device_error(unsigned int* code, int clear);
+
+/* Process-global tuning switches (not thread-safe; for tests and tuning). */
+typedef enum {
+  MLA_OPT_ATTN_PATH = 0,       /* 0 auto, 1 force warp path, 2 force tensor-core path */
+  MLA_OPT_KV_SPLITS = 1,       /* 0 auto, n > 0 split the key range into n parts      */
+  MLA_OPT_PREFILL_FUSED = 2    /* 1 (default) per-head fused kernel for long prefill,
+                                  0 always the head-packed kernels                    */
+} mla_option_t;
+mla_status_t mla_set_option(int option, int64_t value);
+
+/* Human-readable name of a status code (static string). */
+const char* mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */

@@ -1,0 +1,156 @@
+"""Latent causal attention for GB300 (sm_103a): Python binding of the C ABI.
+
+Every call below only marshals torch tensors (device memory, the current CUDA
+stream) into the C functions declared in include/mla.h; all arithmetic runs
+in the library's CUDA kernels.  There is no CPU fallback: without the built
+library or without a GPU the calls raise.
+
+    project(hidden, w_down, w_up_k=None, w_up_v=None)  -> latent, k, v
+    attention(q, kv_latent, w_up_k, w_up_v, scale, causal=True) -> out
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import MLAError, MLA_BF16, MLA_F32
+
+__all__ = ["project", "attention", "attention_from_host", "workspace_size", "merge_partials",
+           "set_option", "device_error", "MLAError", "dtype_code"]
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return MLA_F32
+    if dt == torch.bfloat16:
+        return MLA_BF16
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def project(hidden: torch.Tensor, w_down: torch.Tensor, w_up_k: Optional[torch.Tensor] = None,
+            w_up_v: Optional[torch.Tensor] = None, *, out_dtype: Optional[torch.dtype] = None,
+            latent: Optional[torch.Tensor] = None
+            ) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
+    """latent = hidden @ w_down; k = latent @ w_up_k; v = latent @ w_up_v.
+
+    hidden (..., model_dim); w_down (model_dim, rank); w_up_k / w_up_v
+    (rank, kv_dim) or (rank, H, d).  Returns latent (..., rank) and k, v
+    (..., kv_dim) (None where the weight is None)."""
+    lib = _lib.load()
+    out_dtype = out_dtype or hidden.dtype
+    Dm, R = w_down.shape
+    lead = hidden.shape[:-1]
+    M = hidden.numel() // Dm
+    kvd = 0
+    for w in (w_up_k, w_up_v):
+        if w is not None:
+            kvd = w.numel() // R
+    dev = hidden.device
+    if latent is None:
+        latent = torch.empty(*lead, R, device=dev, dtype=out_dtype)
+    k = torch.empty(*lead, kvd, device=dev, dtype=out_dtype) if w_up_k is not None else None
+    v = torch.empty(*lead, kvd, device=dev, dtype=out_dtype) if w_up_v is not None else None
+    st = lib.mla_kv_latent_project(_ptr(hidden), _ptr(w_down), _ptr(w_up_k), _ptr(w_up_v),
+                                   _ptr(latent), _ptr(k), _ptr(v), M, Dm, R, kvd,
+                                   dtype_code(hidden.dtype), dtype_code(out_dtype), _stream(dev))
+    _lib.check("mla_kv_latent_project", st)
+    return latent, k, v
+
+
+def workspace_size(B: int, Tq: int, Tkv: int, H: int, d: int, rank: int,
+                   dtype: torch.dtype, causal: bool = True) -> int:
+    lib = _lib.load()
+    return int(lib.mla_latent_attention_workspace_size(B, Tq, Tkv, H, d, rank, dtype_code(dtype),
+                                                       int(causal)))
+
+
+def attention(q: torch.Tensor, kv_latent: torch.Tensor, w_up_k: torch.Tensor,
+              w_up_v: torch.Tensor, scale: float, causal: bool = True, *,
+              out_dtype: torch.dtype = torch.float32, out: Optional[torch.Tensor] = None,
+              workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Causal latent attention.  q (B,Tq,H,d), kv_latent (B,Tkv,rank),
+    w_up_k / w_up_v (rank,H,d); returns out (B,Tq,H,d) in ``out_dtype``.
+    ``workspace`` (uint8, at least workspace_size(...) bytes) is allocated
+    here when not given."""
+    lib = _lib.load()
+    B, Tq, H, d = q.shape
+    Tkv, R = kv_latent.shape[1], kv_latent.shape[2]
+    dev = q.device
+    if out is None:
+        out = torch.empty(B, Tq, H, d, device=dev, dtype=out_dtype)
+    ws_bytes = workspace_size(B, Tq, Tkv, H, d, R, q.dtype, causal)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    st = lib.mla_latent_attention(_ptr(q), _ptr(kv_latent), _ptr(w_up_k), _ptr(w_up_v), _ptr(out),
+                                  B, Tq, Tkv, H, d, R, float(scale), int(causal),
+                                  dtype_code(q.dtype), dtype_code(out.dtype), _ptr(workspace),
+                                  0 if workspace is None else workspace.numel(), _stream(dev))
+    _lib.check("mla_latent_attention", st)
+    return out
+
+
+def attention_from_host(q: torch.Tensor, kv_latent: torch.Tensor, w_up_k: torch.Tensor,
+                        w_up_v: torch.Tensor, scale: float, causal: bool = True, *,
+                        device: torch.device, out_dtype: torch.dtype = torch.float32,
+                        dev_buffers: Optional[dict] = None) -> torch.Tensor:
+    """The same call for inputs in (pinned) host memory: copies the inputs to
+    the device, runs the attention and copies the result back; returns a host
+    tensor.  ``dev_buffers`` may hold preallocated device tensors keyed by
+    name to avoid allocation per call."""
+    bufs = dev_buffers if dev_buffers is not None else {}
+    dq = bufs.get("q") if "q" in bufs else torch.empty_like(q, device=device)
+    dl = bufs.get("kv_latent") if "kv_latent" in bufs else torch.empty_like(kv_latent, device=device)
+    dk = bufs.get("w_up_k") if "w_up_k" in bufs else torch.empty_like(w_up_k, device=device)
+    dv = bufs.get("w_up_v") if "w_up_v" in bufs else torch.empty_like(w_up_v, device=device)
+    dq.copy_(q, non_blocking=True)
+    dl.copy_(kv_latent, non_blocking=True)
+    dk.copy_(w_up_k, non_blocking=True)
+    dv.copy_(w_up_v, non_blocking=True)
+    out = attention(dq, dl, dk, dv, scale, causal, out_dtype=out_dtype, out=bufs.get("out"),
+                    workspace=bufs.get("workspace"))
+    host = bufs.get("host_out")
+    if host is None:
+        host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    host.copy_(out, non_blocking=True)
+    return host
+
+
+def merge_partials(m: torch.Tensor, l: torch.Tensor, o: torch.Tensor,
+                   out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    """Split-KV merge of partial softmax states: m, l (parts, rows) fp32 in log2
+    units, o (parts, rows, width) fp32 -> (rows, width)."""
+    lib = _lib.load()
+    parts, rows, width = o.shape
+    out = torch.empty(rows, width, device=o.device, dtype=out_dtype)
+    st = lib.mla_merge_partials(_ptr(m), _ptr(l), _ptr(o), _ptr(out), parts, rows, width,
+                                dtype_code(out_dtype), _stream(o.device))
+    _lib.check("mla_merge_partials", st)
+    return out
+
+
+def set_option(option: int, value: int) -> None:
+    _lib.check("mla_set_option", _lib.load().mla_set_option(option, value))
+
+
+def device_error(clear: bool = False) -> int:
+    code = ctypes.c_uint(0)
+    _lib.check("mla_get_device_error", _lib.load().mla_get_device_error(ctypes.byref(code),
+                                                                        int(clear)))
+    return code.value

@@ -1,0 +1,487 @@
+// Causal latent attention flash loop for sm_103a (tcgen05 + TMA + TMEM).
+//
+// Definition (page "FW-GLM-5-1 l2_p31", fused MLA-style attention from
+// compressed KV latents, "The algorithm"): for each row (b, t, h),
+//   logit_s = scale * q[b,t,h] . (latent[b,s] @ w_up_k[:,h])   for s <= t,
+//   out = sum_s softmax(logit)_s * (latent[b,s] @ w_up_v[:,h]).
+// The key weights are absorbed into the query beforehand, q' = w_up_k[:,h] q
+// (length rank, pre-multiplied by scale * log2 e), so every head attends the
+// SAME matrix, the latent rows themselves:
+//   S = q' L^T (contraction over rank),  O_lat = softmax(S) L,
+// and w_up_v is applied to O_lat afterwards, once per output row.  The
+// softmax is the online (running max / running sum / rescaled accumulator)
+// form of page "Kimi-K2.6 l2_p29" (online softmax derivation), evaluated in
+// base 2, with its -inf rules: an entry at -inf contributes 0 and a row with
+// no visible key yet keeps m = -inf without producing NaN.
+//
+// Tile: 128 rows (query position, head) x 64 keys.  The latent tile in shared
+// memory (128-byte swizzle, rank-contiguous rows) feeds both MMAs: K-major as
+// the B operand of S = q' L^T and MN-major as the B operand of O += P L.
+// O_lat (128 x rank fp32) lives in tensor memory.  A 512-wide rank would fill
+// all 512 TMEM columns, so for rank > 256 two CTAs of a cluster split the
+// rank: each holds q', the latent tiles and O_lat for its half, computes a
+// partial S over its half, and the pair exchanges the partial S tiles through
+// distributed shared memory; both then run the identical softmax (the sum of
+// the two partials is the same bits in either CTA) and accumulate their half
+// of O_lat.
+//
+// Warp roles (192 threads): warp 0 lane 0 = TMA producer (q' once, then a
+// 3-stage ring of latent tiles); warp 1 = TMEM owner, lane 0 issues MMAs;
+// warps 2-5 = softmax, one thread per row (warp w reads TMEM lanes
+// 32*(w%4)..+31), and the epilogue.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kRows = 128;           // rows per CTA tile (MMA M)
+constexpr int kKeys = 64;            // keys per tile (S MMA N, O MMA K)
+constexpr int kStages = 3;           // latent tile ring
+constexpr int kMaxRC = 256;          // rank columns per CTA
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
+
+constexpr int kQBytes = kRows * kMaxRC * 2;       // 64 KB
+constexpr int kLStage = kKeys * kMaxRC * 2;       // 32 KB
+constexpr int kPBytes = kRows * kKeys * 2;        // 16 KB
+constexpr int kXBytes = kRows * kKeys * 4;        // 32 KB
+constexpr int kOffQ = 0;
+constexpr int kOffL = kOffQ + kQBytes;
+constexpr int kOffP = kOffL + kStages * kLStage;
+constexpr int kOffX = kOffP + 2 * kPBytes;
+constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;   // + barriers + alignment slack
+
+constexpr uint32_t kTmemO = 0;       // columns [0, RC)
+constexpr uint32_t kTmemS = 256;     // two 64-column S buffers at 256, 320
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t l_full[kStages];
+  uint64_t l_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_empty[2];
+  uint64_t p_full[2];
+  uint64_t p_empty[2];
+  uint64_t o_last;
+  uint64_t x_full;     // my exchange buffer was filled by the peer
+  uint64_t x_empty;    // the peer's exchange buffer may be written again
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Every lane waits, then the warp agrees: a lane that timed out makes the whole
+// warp give up, so warp-collective tcgen05 instructions never see a split warp.
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int site,
+                                          volatile int* abort) {
+  const bool ok = mbar_wait<kCluster>(bar, parity, site, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Position of 16-byte chunk c (0..15) of row r in the 256-byte rows of the
+// exchange buffer; the low three chunk bits are XOR-ed with the row so that
+// eight consecutive rows hit eight different bank groups.
+__device__ __forceinline__ uint32_t x_offset(uint32_t r, uint32_t c) {
+  return r * 256u + (((c & 8u) | ((c ^ r) & 7u)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    flash_packed_kernel(const __grid_constant__ CUtensorMap mapQ,
+                        const __grid_constant__ CUtensorMap mapL, FlashArgs a) {
+  extern __shared__ uint8_t flash_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(flash_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sL = smem + kOffL;
+  uint8_t* sP = smem + kOffP;
+  uint8_t* sX = smem + kOffX;
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int csize = a.pair ? 2 : 1;
+  const uint32_t crank = a.pair ? cluster_ctarank() : 0u;
+  const uint32_t peer = crank ^ 1u;
+
+  // ---- work item: heavy row blocks first ----
+  const int work = blockIdx.x / csize;
+  const int per_rb = a.B * a.splits;
+  const int rb = a.row_blocks - 1 - work / per_rb;
+  const int b = (work / a.splits) % a.B;
+  const int sp = work % a.splits;
+  const int rows_b = a.Tq * a.H;
+  const int row0 = rb * kRows;
+  const int last_row = min(row0 + kRows, rows_b) - 1;
+  const int t_max = a.Tkv - a.Tq + last_row / a.H;
+  const int kv_len = a.causal ? min(t_max + 1, a.Tkv) : a.Tkv;
+  const int n_tiles_all = (kv_len + kKeys - 1) / kKeys;
+  const int per_split = (n_tiles_all + a.splits - 1) / a.splits;
+  const int tile0 = sp * per_split;
+  const int nt = max(0, min(n_tiles_all, tile0 + per_split) - tile0);
+  const int RC = a.RC;
+  const int c0 = (int)crank * RC;          // first rank column of this CTA
+  const int nchunk = RC / 64;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->l_full[s], 1);
+      mbar_init(&bars->l_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_empty[i], 128);
+      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->p_empty[i], 1);
+    }
+    mbar_init(&bars->o_last, 1);
+    mbar_init(&bars->x_full, 128);
+    mbar_init(&bars->x_empty, 128);
+    bars->abort_flag = 0;
+    fence_mbarrier_init_cluster();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  if (a.pair) cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0 && nt > 0) {
+      prefetch_tensormap(&mapQ);
+      prefetch_tensormap(&mapL);
+      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
+      for (int kc = 0; kc < nchunk; ++kc)
+        tma_load_3d(sQ + kc * (kRows * 128), &mapQ, &bars->q_full, c0 + 64 * kc, row0, b);
+      int issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int st = j % kStages;
+        if (!mbar_wait(&bars->l_empty[st], ((j / kStages) & 1) ^ 1, 10, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(kKeys * RC * 2));
+        uint8_t* dst = sL + st * kLStage;
+        for (int kc = 0; kc < nchunk; ++kc)
+          tma_load_3d(dst + kc * (kKeys * 128), &mapL, &bars->l_full[st], c0 + 64 * kc,
+                      (tile0 + j) * kKeys, b);
+        ++issued;
+      }
+      // Do not leave copies in flight: wait for the last loads of each stage.
+      for (int j = max(0, issued - kStages); j < issued; ++j)
+        mbar_wait(&bars->l_full[j % kStages], (j / kStages) & 1, 11, nullptr);
+      mbar_wait(&bars->q_full, 0, 12, nullptr);
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0 && nt > 0) {
+      const uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
+      const uint32_t idesc_o = make_idesc_bf16(kRows, RC, false, true);
+      const uint32_t q0 = smem_u32(sQ), l0 = smem_u32(sL), p0 = smem_u32(sP);
+      bool ok = mbar_wait(&bars->q_full, 0, 20, abort_flag);
+      auto issue_o = [&](int jj) -> bool {
+        if (!mbar_wait(&bars->p_full[jj & 1], (jj >> 1) & 1, 21, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t lst = l0 + (jj % kStages) * kLStage;
+        const uint32_t pb = p0 + (jj & 1) * kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t ad = make_sdesc_sw128(pb + kk * 32, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(lst + kk * 2048, kKeys * 128, 1024);
+          umma_bf16(tmem + kTmemO, ad, bd, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars->p_empty[jj & 1]);
+        umma_commit(&bars->l_empty[jj % kStages]);
+        return true;
+      };
+      for (int j = 0; j < nt && ok; ++j) {
+        const int st = j % kStages;
+        if (!mbar_wait(&bars->l_full[st], (j / kStages) & 1, 22, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&bars->s_empty[j & 1], ((j >> 1) & 1) ^ 1, 23, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t lst = l0 + st * kLStage;
+        const uint32_t sbuf = tmem + kTmemS + (j & 1) * kKeys;
+        for (int k = 0; k < RC / 16; ++k) {
+          const uint32_t kc = k >> 2, kw = k & 3;
+          const uint64_t ad = make_sdesc_sw128(q0 + kc * (kRows * 128) + kw * 32, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(lst + kc * (kKeys * 128) + kw * 32, 16, 1024);
+          umma_bf16(sbuf, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->s_full[j & 1]);
+        if (j > 0 && !issue_o(j - 1)) { ok = false; break; }
+      }
+      if (ok) issue_o(nt - 1);
+      umma_commit(&bars->o_last);
+    }
+  } else {
+    // ======================= softmax / epilogue =======================
+    const int qd = warp & 3;                      // TMEM lane quadrant
+    const int r = qd * 32 + lane;                 // row within the tile
+    const int grow = row0 + r;                    // row within batch entry b
+    const bool row_valid = grow < rows_b;
+    const int t_row = a.Tkv - a.Tq + (row_valid ? grow / a.H : 0);
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const uint32_t x_local = smem_u32(sX);
+    const uint32_t x_peer = a.pair ? mapa_shared(x_local, peer) : 0u;
+    const uint32_t xfull_peer = a.pair ? mapa_shared(smem_u32(&bars->x_full), peer) : 0u;
+    const uint32_t xempty_peer = a.pair ? mapa_shared(smem_u32(&bars->x_empty), peer) : 0u;
+
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt && ok; ++j) {
+      float s[kKeys];
+      if (!warp_wait(&bars->s_full[j & 1], (j >> 1) & 1, 30, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      {
+        float* s0 = s;
+        float(&a0)[32] = *reinterpret_cast<float(*)[32]>(s0);
+        float(&a1)[32] = *reinterpret_cast<float(*)[32]>(s0 + 32);
+        const uint32_t sb = tmem + lane_base + kTmemS + (j & 1) * kKeys;
+        tmem_ld32(sb, a0);
+        tmem_ld32(sb + 32, a1);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->s_empty[j & 1]);
+
+      if (a.pair) {
+        // partial S over my half of the rank -> peer; peer's partial -> mine
+        if (!warp_wait<true>(&bars->x_empty, (j & 1) ^ 1, 31, abort_flag)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_cluster_v4(x_peer + x_offset(r, c), s[4 * c], s[4 * c + 1], s[4 * c + 2],
+                        s[4 * c + 3]);
+        mbar_arrive_remote(xfull_peer);
+        if (!warp_wait<true>(&bars->x_full, j & 1, 32, abort_flag)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float x0, x1, x2, x3;
+          ld_shared_v4f(x_local + x_offset(r, c), x0, x1, x2, x3);
+          s[4 * c] += x0;
+          s[4 * c + 1] += x1;
+          s[4 * c + 2] += x2;
+          s[4 * c + 3] += x3;
+        }
+        mbar_arrive_remote(xempty_peer);
+      }
+
+      // mask: key s_idx visible iff s_idx < Tkv and (not causal or s_idx <= t)
+      const int key0 = (tile0 + j) * kKeys;
+      const int lim = a.causal ? min(t_row + 1, a.Tkv) : a.Tkv;   // visible keys < lim
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) {
+        if (!row_valid || key0 + c >= lim) s[c] = -INFINITY;
+        mx = fmaxf(mx, s[c]);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const bool grow_max = m_new > m_run + kRescaleThreshold;   // false while both -inf
+      const float m_ref = grow_max ? m_new : m_run;
+      const float alpha = grow_max ? ex2(m_run - m_new) : 1.f;   // m_run = -inf -> 0
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) {
+        s[c] = ex2(s[c] - m_use);
+        psum += s[c];
+      }
+      l_run = l_run * alpha + psum;
+      m_run = m_ref;
+
+      // rescale O_lat (only after the previous P.L has landed)
+      if (__any_sync(0xffffffffu, grow_max && j > 0)) {
+        if (!warp_wait(&bars->p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, 33, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int c = 0; c < RC; c += 32) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + kTmemO + c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tmem + lane_base + kTmemO + c, o);
+        }
+        tmem_wait_st();
+      }
+
+      // P (bf16) into the K-major swizzled P buffer
+      if (!warp_wait(&bars->p_empty[j & 1], ((j >> 1) & 1) ^ 1, 34, abort_flag)) { ok = false; break; }
+      const uint32_t pb = smem_u32(sP + (j & 1) * kPBytes);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(pb + sw128_offset(r, c), pack_bf16x2(s[8 * c], s[8 * c + 1]),
+                     pack_bf16x2(s[8 * c + 2], s[8 * c + 3]),
+                     pack_bf16x2(s[8 * c + 4], s[8 * c + 5]),
+                     pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[j & 1]);
+    }
+
+    // ---------------- epilogue ----------------
+    const int64_t gr = (int64_t)b * rows_b + grow;     // row in (B*Tq*H)
+    const int64_t nrows = (int64_t)a.B * rows_b;
+    bool have_o = false;
+    if (ok && nt > 0) {
+      have_o = warp_wait(&bars->o_last, 0, 35, abort_flag);
+      __syncwarp();
+      tc_fence_after();
+    }
+    if (a.splits == 1) {
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.olat) + gr * a.R + c0;
+      for (int c = 0; c < RC; c += 32) {
+        float o[32];
+        if (have_o) {
+          tmem_ld32(tmem + lane_base + kTmemO + c, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (row_valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                               pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                               pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                               pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+        }
+      }
+    } else {
+      float* dst = a.part_o + ((int64_t)sp * nrows + gr) * a.R + c0;
+      for (int c = 0; c < RC; c += 32) {
+        float o[32];
+        if (have_o) {
+          tmem_ld32(tmem + lane_base + kTmemO + c, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (row_valid) {
+          float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
+      if (row_valid && crank == 0) {
+        float* ml = a.part_ml + ((int64_t)sp * nrows + gr) * 2;
+        ml[0] = have_o ? m_run : -INFINITY;
+        ml[1] = have_o ? l_run : 0.f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (a.pair) cluster_sync();
+}
+
+// ---------------------------------------------------------------------------
+// Split-KV merge: out[r,:] = sum_p 2^(m_p - M) o_p[r,:] / sum_p 2^(m_p - M) l_p
+// (page "Kimi-K2.6 l2_p29", online softmax, applied to whole partitions).
+// One block of width/4 threads per row, float4 per thread.
+// ---------------------------------------------------------------------------
+__global__ void merge_partials_kernel(const float* __restrict__ ml, int ml_stride,
+                                      const float* __restrict__ lsep,
+                                      const float* __restrict__ o, void* __restrict__ out,
+                                      int parts, int rows, int width, int out_bf16) {
+  const int row = blockIdx.x;
+  if (row >= rows) return;
+  // m of part p at ml[(p*rows + row)*ml_stride]; l at +1 (or lsep[p*rows+row]).
+  float M = -INFINITY;
+  for (int p = 0; p < parts; ++p) M = fmaxf(M, ml[((int64_t)p * rows + row) * ml_stride]);
+  float lsum = 0.f;
+  for (int p = 0; p < parts; ++p) {
+    const float mp = ml[((int64_t)p * rows + row) * ml_stride];
+    const float lp = lsep ? lsep[(int64_t)p * rows + row]
+                          : ml[((int64_t)p * rows + row) * ml_stride + 1];
+    if (mp != -INFINITY) lsum += ex2(mp - M) * lp;
+  }
+  const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+  for (int c = threadIdx.x * 4; c < width; c += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < parts; ++p) {
+      const float mp = ml[((int64_t)p * rows + row) * ml_stride];
+      if (mp == -INFINITY) continue;
+      const float w = ex2(mp - M);
+      const float4 v = *reinterpret_cast<const float4*>(o + ((int64_t)p * rows + row) * width + c);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    if (out_bf16) {
+      uint2 pk = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
+                            pack_bf16x2(acc.z * inv, acc.w * inv));
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + (int64_t)row * width + c) = pk;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + (int64_t)row * width + c) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                const FlashArgs& args, cudaStream_t stream) {
+  auto kern = flash_packed_kernel;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int csize = args.pair ? 2 : 1;
+  const unsigned blocks = (unsigned)(args.row_blocks * args.B * args.splits * csize);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t flash_read_device_error(unsigned int* code, int clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned int));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
+  }
+  return e;
+}
+
+cudaError_t launch_merge_partials(const float* ml, int ml_stride, const float* l, const float* o,
+                                  void* out, int parts, int rows, int width, int out_bf16,
+                                  cudaStream_t stream) {
+  const int threads = min(256, max(32, ((width / 4 + 31) / 32) * 32));
+  merge_partials_kernel<<<rows, threads, 0, stream>>>(ml, ml_stride, l, o, out, parts, rows,
+                                                      width, out_bf16);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

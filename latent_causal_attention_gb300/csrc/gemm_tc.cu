@@ -1,0 +1,178 @@
+// Tensor-core GEMM for sm_103a: TMA-staged 128-byte-swizzled tiles, tcgen05.mma
+// (kind::f16, bf16 inputs, fp32 accumulate) into tensor memory, tcgen05.ld
+// epilogue.  One CTA computes one 128 x BN tile of one group.
+//
+// It serves three steps of the path, all plain contractions:
+//   - the down-projection latent = hidden @ w_down (page "FW-GLM-5-1 l2_p1",
+//     problem statement) and the optional k / v up-projections;
+//   - the query absorption q'[., h, :] = w_up_k[:, h, :] q[., h, :] (one group
+//     per head);
+//   - the value up-projection out[., h, :] = o_lat[., h, :] @ w_up_v[:, h, :].
+//
+// Warp roles (128 threads): warp 0 lane 0 issues TMA loads into a 4-stage
+// ring, warp 1 owns the tensor memory and its lane 0 issues the MMAs; all four
+// warps then drain the accumulator (warp w reads TMEM lanes 32w..32w+31).
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kBM = 128, kBK = 64, kStages = 4, kThreads = 128;
+constexpr int kAStage = kBM * kBK * 2;      // 16 KB
+constexpr int kBStage = 256 * kBK * 2;      // 32 KB (BN <= 256)
+constexpr int kSmemBytes = kStages * (kAStage + kBStage) + 256 + 1024;
+
+template <bool kBMN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
+                   const __grid_constant__ CUtensorMap mapB, GemmArgs g) {
+  extern __shared__ uint8_t gemm_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kAStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBStage);
+  uint64_t* empty = full + kStages;
+  uint64_t* accum = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BN = g.BN;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kBM, grp = blockIdx.z;
+  const int kblocks = g.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init_cluster();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    prefetch_tensormap(&mapA);
+    prefetch_tensormap(&mapB);
+    const uint32_t bytes = (uint32_t)(kAStage + BN * kBK * 2);
+    int issued = 0;
+    for (int kb = 0; kb < kblocks; ++kb) {
+      const int s = kb % kStages;
+      if (!mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, 1, abort_flag)) break;
+      ++issued;
+      mbar_arrive_expect_tx(&full[s], bytes);
+      tma_load_3d(sA + s * kAStage, &mapA, &full[s], kb * kBK, grp, m0);
+      if (!kBMN) {
+        tma_load_3d(sB + s * kBStage, &mapB, &full[s], kb * kBK, grp, n0);
+      } else {
+        for (int c = 0; c < BN / 64; ++c)
+          tma_load_3d(sB + s * kBStage + c * (kBK * 128), &mapB, &full[s], n0 + 64 * c, grp,
+                      kb * kBK);
+      }
+    }
+    // Do not leave copies in flight: wait for the last load of each stage.
+    for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
+      mbar_wait(&full[kb % kStages], (kb / kStages) & 1, 4, nullptr);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc = make_idesc_bf16(kBM, BN, false, kBMN);
+    bool ok = true;
+    for (int kb = 0; kb < kblocks && ok; ++kb) {
+      const int s = kb % kStages;
+      if (!mbar_wait(&full[s], (kb / kStages) & 1, 2, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sA + s * kAStage);
+      const uint32_t b0 = smem_u32(sB + s * kBStage);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint64_t ad = make_sdesc_sw128(a0 + kk * 32, 16, 1024);
+        const uint64_t bd = kBMN ? make_sdesc_sw128(b0 + kk * 2048, kBK * 128, 1024)
+                                 : make_sdesc_sw128(b0 + kk * 32, 16, 1024);
+        umma_bf16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+      }
+      umma_commit(&empty[s]);
+    }
+    umma_commit(accum);
+  }
+  __syncwarp();
+
+  // ---------------- epilogue: TMEM -> registers -> global ----------------
+  const bool ok = mbar_wait(accum, 0, 3, abort_flag);
+  __syncwarp();
+  tc_fence_after();
+  if (ok) {
+    const int row = m0 + warp * 32 + lane;
+    const bool valid = row < g.M;
+    const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      tmem_ld32(tbase + c * 32, v);
+      tmem_wait_ld();
+      if (valid) {
+        const int64_t off = (int64_t)grp * g.c_gs + (int64_t)row * g.c_rs + n0 + c * 32;
+        if (g.c_bf16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g.C) + off);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pack_bf16x2(v[8 * q] * g.alpha, v[8 * q + 1] * g.alpha),
+                                pack_bf16x2(v[8 * q + 2] * g.alpha, v[8 * q + 3] * g.alpha),
+                                pack_bf16x2(v[8 * q + 4] * g.alpha, v[8 * q + 5] * g.alpha),
+                                pack_bf16x2(v[8 * q + 6] * g.alpha, v[8 * q + 7] * g.alpha));
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(g.C) + off);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(v[4 * q] * g.alpha, v[4 * q + 1] * g.alpha,
+                                 v[4 * q + 2] * g.alpha, v[4 * q + 3] * g.alpha);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+}  // namespace
+
+cudaError_t gemm_read_device_error(unsigned int* code, int clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned int));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
+  }
+  return e;
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap& mapA, const CUtensorMap& mapB, bool b_mn_major,
+                           const GemmArgs& args, cudaStream_t stream) {
+  dim3 grid(args.N / args.BN, (args.M + kBM - 1) / kBM, args.G);
+  if (b_mn_major) {
+    auto k = gemm_tc_kernel<true>;
+    cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, args);
+  } else {
+    auto k = gemm_tc_kernel<false>;
+    cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, args);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mla

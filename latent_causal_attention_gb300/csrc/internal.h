@@ -1,0 +1,72 @@
+// Internal launchers shared by the C-ABI layer (mla_abi.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int kNumSMsHint = 152;
+
+// ----- CUDA-core paths ------------------------------------------------------
+cudaError_t launch_warp_attention(const void* q, const void* lat, const void* wk, const void* wv,
+                                  void* out, int B, int Tq, int Tkv, int H, int d, int R,
+                                  float scale, int causal, int in_bf16, int out_bf16,
+                                  cudaStream_t stream);
+
+cudaError_t launch_projection_cuda_core(const void* hidden, const void* w_down,
+                                        const void* w_up_k, const void* w_up_v, void* latent,
+                                        void* k, void* v, int64_t M, int Dm, int R, int C,
+                                        int in_bf16, int out_bf16, cudaStream_t stream);
+
+// ----- tensor-core GEMM -----------------------------------------------------
+// C[g][m, n] = alpha * sum_k A[g][m, k] * B[g][k, n]   (bf16 in, fp32 accumulate)
+//   A: 3-D tensor map {K, G, M}, box {64, 1, 128}, 128-byte swizzle (K-major).
+//   B: K-major  -> tensor map {K, G, N}, box {64, 1, BN};
+//      MN-major -> tensor map {N, G, K}, box {64, 1, 64}.
+//   C: element (g, m, n) at C + g*c_gs + m*c_rs + n, fp32 or bf16.
+struct GemmArgs {
+  int M, N, K, G;
+  int BN;            // 64, 128 or 256; divides N
+  float alpha;
+  void* C;
+  int c_bf16;
+  int64_t c_rs, c_gs;
+};
+cudaError_t launch_gemm_tc(const CUtensorMap& mapA, const CUtensorMap& mapB, bool b_mn_major,
+                           const GemmArgs& args, cudaStream_t stream);
+
+// ----- flash loop over latent tiles (head-packed rows) ----------------------
+// Rows of one batch entry are (i, h) pairs, r = i*H + h, of the absorbed query
+// q' (bf16, already multiplied by scale*log2 e).  Each CTA (or CTA pair,
+// splitting the rank) runs 128 rows against a contiguous range of 64-key tiles.
+struct FlashArgs {
+  int B, Tq, Tkv, H, R;
+  int RC;            // rank columns per CTA (R, or R/2 with a CTA pair)
+  int pair;          // 1: cluster of two CTAs splitting the rank
+  int row_blocks;    // ceil(Tq*H / 128)
+  int splits;        // key-range partitions
+  int causal;
+  void* olat;        // splits == 1: normalised latent-space output, bf16 (B*Tq*H, R)
+  float* part_o;     // splits > 1: (splits, B*Tq*H, R) unnormalised
+  float* part_ml;    // splits > 1: (splits, B*Tq*H, 2) = (max in log2 units, sum)
+};
+cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                const FlashArgs& args, cudaStream_t stream);
+
+cudaError_t launch_merge_partials(const float* m_l, int ml_stride, const float* l, const float* o,
+                                  void* out, int parts, int rows, int width, int out_bf16,
+                                  cudaStream_t stream);
+
+// Device-side error words (one per translation unit with bounded waits).
+cudaError_t gemm_read_device_error(unsigned int* code, int clear);
+cudaError_t flash_read_device_error(unsigned int* code, int clear);
+
+// ----- helpers ---------------------------------------------------------------
+// 3-D bf16/fp32 tensor map, dims innermost first, strides in bytes for dims 1, 2.
+bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t d0, uint64_t d1,
+                  uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2,
+                  bool swizzle128);
+
+}  // namespace mla

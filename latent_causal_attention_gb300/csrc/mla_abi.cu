@@ -1,0 +1,344 @@
+// C ABI of the library (declared in include/mla.h): argument validation,
+// choice of path, tensor-map construction and kernel launches on the caller's
+// stream.  No allocation, no host synchronisation, no exceptions.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/mla.h"
+#include "internal.h"
+
+namespace mla {
+
+// ---------------------------------------------------------------------------
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t d0, uint64_t d1,
+                  uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2,
+                  bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Options
+// ---------------------------------------------------------------------------
+static int g_attn_path = 0;     // 0 auto, 1 warp, 2 tensor core
+static int g_kv_splits = 0;     // 0 auto
+
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+static int pick_bn(int N) {
+  if (N % 256 == 0) return 256;
+  if (N % 128 == 0) return 128;
+  return 64;
+}
+
+// ---------------------------------------------------------------------------
+// Attention path planning (shared by the workspace query and the call)
+// ---------------------------------------------------------------------------
+struct AttnPlan {
+  bool tc;
+  int pair, RC, row_blocks, splits;
+  int64_t rows;           // B*Tq*H
+  size_t off_qp, off_olat, off_po, off_pml, total;
+};
+
+static bool tc_shape_ok(int d, int R) {
+  if (d % 64 != 0 || d > 256) return false;
+  if (R % 64 != 0 || R > 512) return false;
+  if (R > 256 && (R % 128 != 0)) return false;
+  return true;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static AttnPlan plan_attention(int B, int Tq, int Tkv, int H, int d, int R, int in_dtype,
+                               int causal) {
+  AttnPlan p = {};
+  const bool shape_tc = in_dtype == MLA_BF16 && tc_shape_ok(d, R);
+  p.tc = (g_attn_path == 2) ? shape_tc : (g_attn_path == 1 ? false : shape_tc);
+  if (!p.tc) return p;
+  p.pair = R > 256 ? 1 : 0;
+  p.RC = p.pair ? R / 2 : R;
+  p.rows = (int64_t)B * Tq * H;
+  p.row_blocks = (int)((int64_t)Tq * H + 127) / 128;
+  const int csize = p.pair ? 2 : 1;
+  const int64_t ctas = (int64_t)p.row_blocks * B * csize;
+  const int kv_tiles = (Tkv + 63) / 64;
+  int splits = 1;
+  if (g_kv_splits > 0) {
+    splits = g_kv_splits;
+  } else if (ctas < kNumSMsHint / 2) {
+    splits = (int)((kNumSMsHint + ctas - 1) / ctas);
+  }
+  if (splits > kv_tiles) splits = kv_tiles;
+  if (splits < 1) splits = 1;
+  (void)causal;
+  p.splits = splits;
+  size_t off = 0;
+  p.off_qp = off;   off = align256(off + (size_t)p.rows * R * 2);
+  p.off_olat = off; off = align256(off + (size_t)p.rows * R * 2);
+  if (splits > 1) {
+    p.off_po = off;  off = align256(off + (size_t)splits * p.rows * R * 4);
+    p.off_pml = off; off = align256(off + (size_t)splits * p.rows * 2 * 4);
+  }
+  p.total = off;
+  return p;
+}
+
+static mla_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_NULL: return "null pointer";
+    case MLA_ERR_SHAPE: return "invalid shape";
+    case MLA_ERR_DTYPE: return "unsupported dtype";
+    case MLA_ERR_ALIGN: return "misaligned pointer";
+    case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_TIMEOUT: return "device-side wait timed out";
+    case MLA_ERR_UNSUPPORTED: return "unsupported by this build";
+    default: return "unknown status";
+  }
+}
+
+mla_status_t mla_set_option(int option, int64_t value) {
+  switch (option) {
+    case MLA_OPT_ATTN_PATH:
+      if (value < 0 || value > 2) return MLA_ERR_SHAPE;
+      g_attn_path = (int)value;
+      return MLA_OK;
+    case MLA_OPT_KV_SPLITS:
+      if (value < 0 || value > 4096) return MLA_ERR_SHAPE;
+      g_kv_splits = (int)value;
+      return MLA_OK;
+    default:
+      return MLA_ERR_UNSUPPORTED;
+  }
+}
+
+mla_status_t mla_get_device_error(unsigned int* code, int clear) {
+  if (!code) return MLA_ERR_NULL;
+  unsigned int a = 0, b = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  if (gemm_read_device_error(&a, clear) != cudaSuccess) return MLA_ERR_CUDA;
+  if (flash_read_device_error(&b, clear) != cudaSuccess) return MLA_ERR_CUDA;
+  *code = a ? a : b;
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------------------
+mla_status_t mla_kv_latent_project(const void* hidden, const void* w_down, const void* w_up_k,
+                                   const void* w_up_v, void* latent, void* k, void* v,
+                                   int64_t M, int model_dim, int rank, int kv_dim, int in_dtype,
+                                   int out_dtype, void* stream_) {
+  if (!hidden || !w_down || !latent) return MLA_ERR_NULL;
+  if ((k && !w_up_k) || (v && !w_up_v)) return MLA_ERR_NULL;
+  if (M <= 0 || model_dim <= 0 || rank <= 0) return MLA_ERR_SHAPE;
+  if ((k || v) && kv_dim <= 0) return MLA_ERR_SHAPE;
+  if (M > (int64_t)1 << 31) return MLA_ERR_SHAPE;
+  if (in_dtype != MLA_F32 && in_dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (in_dtype == MLA_F32 && out_dtype != MLA_F32) return MLA_ERR_DTYPE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const bool want_kv = (k != nullptr) || (v != nullptr);
+
+  const bool tc = in_dtype == MLA_BF16 && model_dim % 64 == 0 && rank % 64 == 0 && rank <= 512 &&
+                  (!want_kv || (kv_dim % 64 == 0 && out_dtype == MLA_BF16)) &&
+                  aligned16(hidden) && aligned16(w_down) && aligned16(latent) &&
+                  (!k || (aligned16(k) && aligned16(w_up_k))) &&
+                  (!v || (aligned16(v) && aligned16(w_up_v)));
+  if (!tc) {
+    if (rank > 512) return MLA_ERR_UNSUPPORTED;
+    return cuda_status(launch_projection_cuda_core(hidden, w_down, w_up_k, w_up_v, latent, k, v, M,
+                                                   model_dim, rank, want_kv ? kv_dim : 0,
+                                                   in_dtype == MLA_BF16, out_dtype == MLA_BF16,
+                                                   stream));
+  }
+  // Stage 1: latent = hidden @ w_down  (A K-major, B = w_down MN-major).
+  CUtensorMap mA, mB;
+  if (!make_tmap_3d(&mA, hidden, 2, model_dim, 1, M, (uint64_t)model_dim * 2,
+                    (uint64_t)model_dim * 2, 64, 1, 128, true))
+    return MLA_ERR_CUDA;
+  if (!make_tmap_3d(&mB, w_down, 2, rank, 1, model_dim, (uint64_t)rank * 2, (uint64_t)rank * 2, 64,
+                    1, 64, true))
+    return MLA_ERR_CUDA;
+  GemmArgs g = {};
+  g.M = (int)M; g.N = rank; g.K = model_dim; g.G = 1; g.BN = pick_bn(rank); g.alpha = 1.f;
+  g.C = latent; g.c_bf16 = out_dtype == MLA_BF16; g.c_rs = rank; g.c_gs = 0;
+  cudaError_t e = launch_gemm_tc(mA, mB, true, g, stream);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  if (!want_kv) return MLA_OK;
+  // Stage 2: k / v = latent(bf16) @ w_up_k / w_up_v.
+  CUtensorMap mL;
+  if (!make_tmap_3d(&mL, latent, 2, rank, 1, M, (uint64_t)rank * 2, (uint64_t)rank * 2, 64, 1,
+                    128, true))
+    return MLA_ERR_CUDA;
+  const void* ws[2] = {w_up_k, w_up_v};
+  void* outs[2] = {k, v};
+  for (int i = 0; i < 2; ++i) {
+    if (!outs[i]) continue;
+    CUtensorMap mW;
+    if (!make_tmap_3d(&mW, ws[i], 2, kv_dim, 1, rank, (uint64_t)kv_dim * 2, (uint64_t)kv_dim * 2,
+                      64, 1, 64, true))
+      return MLA_ERR_CUDA;
+    GemmArgs g2 = {};
+    g2.M = (int)M; g2.N = kv_dim; g2.K = rank; g2.G = 1; g2.BN = pick_bn(kv_dim); g2.alpha = 1.f;
+    g2.C = outs[i]; g2.c_bf16 = 1; g2.c_rs = kv_dim; g2.c_gs = 0;
+    e = launch_gemm_tc(mL, mW, true, g2, stream);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------------------
+size_t mla_latent_attention_workspace_size(int B, int Tq, int Tkv, int H, int d, int rank,
+                                           int in_dtype, int causal) {
+  if (B <= 0 || Tq <= 0 || Tkv <= 0 || H <= 0 || d <= 0 || rank <= 0 || Tq > Tkv) return 0;
+  AttnPlan p = plan_attention(B, Tq, Tkv, H, d, rank, in_dtype, causal);
+  return p.tc ? p.total : 0;
+}
+
+mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const void* w_up_k,
+                                  const void* w_up_v, void* out, int B, int Tq, int Tkv, int H,
+                                  int d, int rank, float scale, int causal, int in_dtype,
+                                  int out_dtype, void* workspace, size_t workspace_bytes,
+                                  void* stream_) {
+  if (!q || !kv_latent || !w_up_k || !w_up_v || !out) return MLA_ERR_NULL;
+  if (B <= 0 || Tq <= 0 || Tkv <= 0 || H <= 0 || d <= 0 || rank <= 0 || Tq > Tkv)
+    return MLA_ERR_SHAPE;
+  if ((int64_t)B * Tq * H > ((int64_t)1 << 31) || (int64_t)B * Tkv > ((int64_t)1 << 31))
+    return MLA_ERR_SHAPE;
+  if (in_dtype != MLA_F32 && in_dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (in_dtype == MLA_F32 && out_dtype != MLA_F32) return MLA_ERR_DTYPE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+  AttnPlan p = plan_attention(B, Tq, Tkv, H, d, rank, in_dtype, causal);
+  if (p.tc && !(aligned16(q) && aligned16(kv_latent) && aligned16(w_up_k) && aligned16(w_up_v) &&
+                aligned16(out))) {
+    if (g_attn_path == 2) return MLA_ERR_ALIGN;
+    p.tc = false;
+  }
+  if (!p.tc) {
+    if (g_attn_path == 2) return MLA_ERR_UNSUPPORTED;
+    if (rank > 1024 || d > 256) return MLA_ERR_UNSUPPORTED;
+    return cuda_status(launch_warp_attention(q, kv_latent, w_up_k, w_up_v, out, B, Tq, Tkv, H, d,
+                                             rank, scale, causal, in_dtype == MLA_BF16,
+                                             out_dtype == MLA_BF16, stream));
+  }
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  if (workspace_bytes < p.total) return MLA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLA_ERR_ALIGN;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qp = ws + p.off_qp;
+  void* olat = ws + p.off_olat;
+  const int R = rank;
+  const int64_t BT = (int64_t)B * Tq;
+
+  // 1. absorption: q'[(b,i), h, :] = scale*log2(e) * w_up_k[:, h, :] q[(b,i), h, :]
+  CUtensorMap mA, mB;
+  if (!make_tmap_3d(&mA, q, 2, d, H, BT, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 128, true))
+    return MLA_ERR_CUDA;
+  const int bn_abs = pick_bn(R);
+  if (!make_tmap_3d(&mB, w_up_k, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, bn_abs,
+                    true))
+    return MLA_ERR_CUDA;
+  GemmArgs g = {};
+  g.M = (int)BT; g.N = R; g.K = d; g.G = H; g.BN = bn_abs;
+  g.alpha = scale * 1.4426950408889634f;
+  g.C = qp; g.c_bf16 = 1; g.c_rs = (int64_t)H * R; g.c_gs = R;
+  if (launch_gemm_tc(mA, mB, false, g, stream) != cudaSuccess) return MLA_ERR_CUDA;
+
+  // 2. flash loop over the latent
+  CUtensorMap mQ, mL;
+  if (!make_tmap_3d(&mQ, qp, 2, R, (uint64_t)Tq * H, B, (uint64_t)R * 2,
+                    (uint64_t)Tq * H * R * 2, 64, 128, 1, true))
+    return MLA_ERR_CUDA;
+  if (!make_tmap_3d(&mL, kv_latent, 2, R, Tkv, B, (uint64_t)R * 2, (uint64_t)Tkv * R * 2, 64, 64, 1,
+                    true))
+    return MLA_ERR_CUDA;
+  FlashArgs fa = {};
+  fa.B = B; fa.Tq = Tq; fa.Tkv = Tkv; fa.H = H; fa.R = R; fa.RC = p.RC; fa.pair = p.pair;
+  fa.row_blocks = p.row_blocks; fa.splits = p.splits; fa.causal = causal ? 1 : 0;
+  fa.olat = olat;
+  fa.part_o = p.splits > 1 ? reinterpret_cast<float*>(ws + p.off_po) : nullptr;
+  fa.part_ml = p.splits > 1 ? reinterpret_cast<float*>(ws + p.off_pml) : nullptr;
+  if (launch_flash_packed(mQ, mL, fa, stream) != cudaSuccess) return MLA_ERR_CUDA;
+
+  // 3. merge the key-range partitions
+  if (p.splits > 1) {
+    if (launch_merge_partials(fa.part_ml, 2, nullptr, fa.part_o, olat, p.splits, (int)p.rows, R, 1,
+                              stream) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+
+  // 4. value up-projection: out[(b,i), h, :] = o_lat[(b,i), h, :] @ w_up_v[:, h, :]
+  CUtensorMap mO, mV;
+  if (!make_tmap_3d(&mO, olat, 2, R, H, BT, (uint64_t)R * 2, (uint64_t)H * R * 2, 64, 1, 128,
+                    true))
+    return MLA_ERR_CUDA;
+  if (!make_tmap_3d(&mV, w_up_v, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 64, true))
+    return MLA_ERR_CUDA;
+  GemmArgs g2 = {};
+  g2.M = (int)BT; g2.N = d; g2.K = R; g2.G = H; g2.BN = pick_bn(d); g2.alpha = 1.f;
+  g2.C = out; g2.c_bf16 = out_dtype == MLA_BF16; g2.c_rs = (int64_t)H * d; g2.c_gs = d;
+  if (launch_gemm_tc(mO, mV, true, g2, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status_t mla_merge_partials(const float* m, const float* l, const float* o, void* out,
+                                int parts, int rows, int width, int out_dtype, void* stream_) {
+  if (!m || !l || !o || !out) return MLA_ERR_NULL;
+  if (parts <= 0 || rows <= 0 || width <= 0 || width % 4 != 0) return MLA_ERR_SHAPE;
+  if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (!aligned16(o) || !aligned16(out)) return MLA_ERR_ALIGN;
+  return cuda_status(launch_merge_partials(m, 1, l, o, out, parts, rows, width,
+                                           out_dtype == MLA_BF16,
+                                           static_cast<cudaStream_t>(stream_)));
+}
+
+}  // extern "C"

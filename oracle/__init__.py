@@ -68,6 +68,7 @@ class Oracle:
         L.mla_oracle_attention_absorbed.argtypes = L.mla_oracle_attention.argtypes
         L.mla_oracle_attention_rows.argtypes = [_D, _D, _D, _D, _I32, ctypes.c_int, _D] + [
             ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int]
+        L.mla_oracle_attention_absorbed_rows.argtypes = L.mla_oracle_attention_rows.argtypes
         L.mla_oracle_attention_weights.argtypes = [_D, _D, _D] + [ctypes.c_int] * 9 + [
             ctypes.c_double, ctypes.c_int, _D]
         L.mla_oracle_attention_weights.restype = ctypes.c_int
@@ -137,8 +138,12 @@ class Oracle:
 
     def attention_rows(self, q, kv_latent, w_up_k, w_up_v, scale: float,
                        rows: Sequence[Sequence[int]], causal: bool = True,
-                       prepared=None):
-        """Literal form for selected (b, i) rows only: returns (n, H, d)."""
+                       prepared=None, form: str = "literal"):
+        """Selected (b, i) rows only, all heads: returns (n, H, d).
+
+        ``form="literal"`` rebuilds k, v per key (the definition as written);
+        ``form="absorbed"`` uses the pinned absorbed identity, far cheaper at
+        rank >> head_dim, for sampled checks of large workloads."""
         if prepared is None:
             prepared = self._attn_args(q, kv_latent, w_up_k, w_up_v)
         q, lat, wk, wv, (B, Tq, Tkv, H, d, R) = prepared
@@ -147,9 +152,10 @@ class Oracle:
         assert (bi[:, 1] >= 0).all() and (bi[:, 1] < Tq).all()
         n = bi.shape[0]
         out = np.empty((n, H, d))
-        self.lib.mla_oracle_attention_rows(self._p(q), self._p(lat), self._p(wk), self._p(wv),
-                                           bi.ctypes.data_as(_I32), n, self._p(out), B, Tq,
-                                           Tkv, H, d, R, float(scale), int(causal))
+        fn = {"literal": self.lib.mla_oracle_attention_rows,
+              "absorbed": self.lib.mla_oracle_attention_absorbed_rows}[form]
+        fn(self._p(q), self._p(lat), self._p(wk), self._p(wv), bi.ctypes.data_as(_I32), n,
+           self._p(out), B, Tq, Tkv, H, d, R, float(scale), int(causal))
         return out
 
     def prepare(self, q, kv_latent, w_up_k, w_up_v):

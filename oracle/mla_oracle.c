@@ -221,6 +221,43 @@ int mla_oracle_attention_weights(const double *q, const double *lat, const doubl
 /*   o_r = sum_s p_s latent_s[r];      out_e = sum_r o_r w_up_v[r,h,e].       */
 /* Used only to check that the identity the GPU path relies on holds.         */
 /* ----------------------------------------------------------------------- */
+static void absorbed_row(const double *q, const double *lat, const double *wk,
+                         const double *wv, int b, int h, int i, int Tq, int Tkv, int H, int d,
+                         int R, double scale, int causal, double *out_row)
+{
+    const int S = last_key(i, Tq, Tkv, causal) + 1;
+    const double *qv = q + (((int64_t)b * Tq + i) * H + h) * d;
+    double *qa = (double *)malloc(sizeof(double) * (size_t)R);
+    double *o = (double *)calloc((size_t)R, sizeof(double));
+    double *x = (double *)malloc(sizeof(double) * (size_t)S);
+    for (int r = 0; r < R; ++r) {
+        double acc = 0.0;
+        for (int e = 0; e < d; ++e) acc += wk[((int64_t)r * H + h) * d + e] * qv[e];
+        qa[r] = acc;
+    }
+    double m = -INFINITY;
+    for (int s = 0; s < S; ++s) {
+        const double *ls = lat + ((int64_t)b * Tkv + s) * R;
+        double acc = 0.0;
+        for (int r = 0; r < R; ++r) acc += qa[r] * ls[r];
+        x[s] = acc * scale;
+        if (x[s] > m) m = x[s];
+    }
+    double Z = 0.0;
+    for (int s = 0; s < S; ++s) { x[s] = exp(x[s] - m); Z += x[s]; }
+    for (int s = 0; s < S; ++s) {
+        const double *ls = lat + ((int64_t)b * Tkv + s) * R;
+        const double p = x[s] / Z;
+        for (int r = 0; r < R; ++r) o[r] += p * ls[r];
+    }
+    for (int e = 0; e < d; ++e) {
+        double acc = 0.0;
+        for (int r = 0; r < R; ++r) acc += o[r] * wv[((int64_t)r * H + h) * d + e];
+        out_row[e] = acc;
+    }
+    free(x); free(o); free(qa);
+}
+
 void mla_oracle_attention_absorbed(const double *q, const double *lat, const double *wk,
                                    const double *wv, double *out, int B, int Tq, int Tkv,
                                    int H, int d, int R, double scale, int causal)
@@ -231,38 +268,22 @@ void mla_oracle_attention_absorbed(const double *q, const double *lat, const dou
         const int h = (int)(n % H);
         const int i = (int)((n / H) % Tq);
         const int b = (int)(n / ((int64_t)H * Tq));
-        const int S = last_key(i, Tq, Tkv, causal) + 1;
-        const double *qv = q + n * d;
-        double *qa = (double *)malloc(sizeof(double) * (size_t)R);
-        double *o = (double *)calloc((size_t)R, sizeof(double));
-        double *x = (double *)malloc(sizeof(double) * (size_t)S);
-        for (int r = 0; r < R; ++r) {
-            double acc = 0.0;
-            for (int e = 0; e < d; ++e) acc += wk[((int64_t)r * H + h) * d + e] * qv[e];
-            qa[r] = acc;
-        }
-        double m = -INFINITY;
-        for (int s = 0; s < S; ++s) {
-            const double *ls = lat + ((int64_t)b * Tkv + s) * R;
-            double acc = 0.0;
-            for (int r = 0; r < R; ++r) acc += qa[r] * ls[r];
-            x[s] = acc * scale;
-            if (x[s] > m) m = x[s];
-        }
-        double Z = 0.0;
-        for (int s = 0; s < S; ++s) { x[s] = exp(x[s] - m); Z += x[s]; }
-        for (int s = 0; s < S; ++s) {
-            const double *ls = lat + ((int64_t)b * Tkv + s) * R;
-            const double p = x[s] / Z;
-            for (int r = 0; r < R; ++r) o[r] += p * ls[r];
-        }
-        for (int e = 0; e < d; ++e) {
-            double acc = 0.0;
-            for (int r = 0; r < R; ++r) acc += o[r] * wv[((int64_t)r * H + h) * d + e];
-            out[n * d + e] = acc;
-        }
-        free(x); free(o); free(qa);
+        absorbed_row(q, lat, wk, wv, b, h, i, Tq, Tkv, H, d, R, scale, causal, out + n * d);
     }
+}
+
+/* Absorbed form for selected (b, i) rows; same layout as the literal rows call. */
+void mla_oracle_attention_absorbed_rows(const double *q, const double *lat, const double *wk,
+                                        const double *wv, const int32_t *bi, int n,
+                                        double *out_rows, int B, int Tq, int Tkv, int H, int d,
+                                        int R, double scale, int causal)
+{
+    (void)B;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int j = 0; j < n; ++j)
+        for (int h = 0; h < H; ++h)
+            absorbed_row(q, lat, wk, wv, bi[2 * j], h, bi[2 * j + 1], Tq, Tkv, H, d, R, scale,
+                         causal, out_rows + ((int64_t)j * H + h) * d);
 }
 
 /* ----------------------------------------------------------------------- */

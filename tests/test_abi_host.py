@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every function include/mla.h declares, and argument validation
+rejects bad calls before anything reaches the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from latent_causal_attention_gb300 import _lib
+from latent_causal_attention_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(mla_[a-z_0-9]+)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_header_declares_the_two_calls():
+    names = declared_functions()
+    assert "mla_kv_latent_project" in names and "mla_latent_attention" in names
+    assert len(names) >= 7
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert lib.mla_status_string(0) == b"ok"
+    assert lib.mla_status_string(5).startswith(b"workspace")
+
+
+P = ctypes.c_void_p(16)      # a non-null, 16-byte aligned dummy (never dereferenced)
+
+
+def attn(lib, **kw):
+    a = dict(q=P, lat=P, wk=P, wv=P, out=P, B=2, Tq=8, Tkv=8, H=2, d=64, R=64, scale=0.1,
+             causal=1, ind=1, outd=0, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.mla_latent_attention(a["q"], a["lat"], a["wk"], a["wv"], a["out"], a["B"], a["Tq"],
+                                    a["Tkv"], a["H"], a["d"], a["R"], a["scale"], a["causal"],
+                                    a["ind"], a["outd"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_attention_validation(lib):
+    assert attn(lib, q=None) == 1
+    assert attn(lib, out=None) == 1
+    assert attn(lib, B=0) == 2
+    assert attn(lib, Tq=9, Tkv=8) == 2            # more queries than keys
+    assert attn(lib, d=-1) == 2
+    assert attn(lib, ind=7) == 3
+    assert attn(lib, ind=0, outd=1) == 3          # fp32 in -> bf16 out is not offered
+    # tensor-core path (bf16, d and rank multiples of 64) needs a workspace
+    assert attn(lib, ws=None, wsb=0) == 5
+    need = lib.mla_latent_attention_workspace_size(2, 8, 8, 2, 64, 64, 1, 1)
+    assert need > 0
+    assert attn(lib, ws=ctypes.c_void_p(256), wsb=need - 1) == 5
+    assert attn(lib, ws=ctypes.c_void_p(16), wsb=need) == 4     # workspace not 256-aligned
+
+
+def test_workspace_size_rules(lib):
+    ws = lib.mla_latent_attention_workspace_size
+    assert ws(2, 32, 32, 4, 16, 24, 0, 1) == 0                 # fp32: warp path, no workspace
+    assert ws(2, 32, 32, 4, 16, 24, 1, 1) == 0                 # bf16, d=16: warp path
+    assert ws(4, 1024, 1024, 16, 64, 256, 1, 1) >= 2 * 4 * 1024 * 16 * 256 * 2
+    assert ws(0, 1, 1, 1, 64, 64, 1, 1) == 0
+    # forcing several key partitions adds the partial buffers
+    base = ws(64, 1, 4096, 128, 128, 512, 1, 1)
+    assert lib.mla_set_option(_lib.OPT_KV_SPLITS, 4) == 0
+    try:
+        assert ws(64, 1, 4096, 128, 128, 512, 1, 1) >= base + 4 * 64 * 128 * 512 * 4
+    finally:
+        lib.mla_set_option(_lib.OPT_KV_SPLITS, 0)
+
+
+def test_project_validation(lib):
+    f = lib.mla_kv_latent_project
+    assert f(None, P, None, None, P, None, None, 8, 64, 64, 0, 0, 0, None) == 1
+    assert f(P, P, None, None, P, P, None, 8, 64, 64, 64, 0, 0, None) == 1   # k without w_up_k
+    assert f(P, P, None, None, P, None, None, 0, 64, 64, 0, 0, 0, None) == 2
+    assert f(P, P, None, None, P, None, None, 8, 64, 64, 0, 0, 1, None) == 3
+
+
+def test_options(lib):
+    assert lib.mla_set_option(0, 3) == 2
+    assert lib.mla_set_option(99, 0) == 8
+    assert lib.mla_set_option(0, 0) == 0
+    assert lib.mla_merge_partials(None, P, P, P, 1, 1, 4, 0, None) == 1
+    assert lib.mla_merge_partials(P, P, P, P, 1, 1, 6, 0, None) == 2
+
+
+def test_product_path_has_no_fallback():
+    """Without the built library the binding raises instead of computing."""
+    with pytest.raises(RuntimeError):
+        _lib.load(path=os.path.join(ROOT, "does_not_exist.so"))

@@ -1,0 +1,234 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Small cases compare every element; the full-size workloads compare sampled
+rows (every head of the chosen (b, i) rows) against the oracle's literal and
+absorbed forms.  Inputs come from the shared seeded generator only.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import latent_causal_attention_gb300 as mla
+from latent_causal_attention_gb300 import _lib
+from latent_causal_attention_gb300.inputs import WORKLOADS, custom_workload, make_inputs
+from oracle import explicit
+
+from _util import assert_bf16_close, assert_f32_close, cuda, sample_rows, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from latent_causal_attention_gb300.build import build
+    build()
+    mla.set_option(_lib.OPT_ATTN_PATH, 0)
+    mla.set_option(_lib.OPT_KV_SPLITS, 0)
+    yield
+    assert mla.device_error() == 0
+
+
+def run_attention(x, w, out_dtype=torch.float32, lat=None):
+    return mla.attention(cuda(x["q"]), cuda(x["kv_latent"]) if lat is None else lat,
+                         cuda(x["w_up_k"]), cuda(x["w_up_v"]), w.scale, w.causal,
+                         out_dtype=out_dtype)
+
+
+# ----------------------------------------------------------------- fp32 workloads
+def test_tiny_f32_full(oracle):
+    w = WORKLOADS["tiny_f32"]
+    x = make_inputs(w)
+    out = run_attention(x, w)
+    ref = oracle.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale)
+    assert_f32_close(out, ref, "tiny_f32")
+
+
+def test_proj_f32_projection_then_attention(oracle):
+    w = WORKLOADS["proj_f32"]
+    x = make_inputs(w)
+    wk2, wv2 = x["w_up_k"].reshape(w.rank, -1), x["w_up_v"].reshape(w.rank, -1)
+    lat, k, v = mla.project(cuda(x["hidden"]), cuda(x["w_down"]), cuda(wk2), cuda(wv2))
+    rl, rk, rv = oracle.project(x["hidden"], x["w_down"], wk2, wv2)
+    assert_f32_close(lat.reshape(-1, w.rank), rl, "latent")
+    assert_f32_close(k.reshape(-1, w.kv_dim), rk, "k")
+    assert_f32_close(v.reshape(-1, w.kv_dim), rv, "v")
+    out = run_attention(x, w, lat=lat)
+    ref = oracle.attention(x["q"], rl.reshape(w.B, w.Tkv, w.rank), x["w_up_k"], x["w_up_v"],
+                           w.scale)
+    assert_f32_close(out, ref, "proj_f32 attention")
+
+
+@pytest.mark.parametrize("shape", [
+    dict(B=2, Tq=9, Tkv=13, H=3, d=5, rank=7, causal=True),
+    dict(B=1, Tq=1, Tkv=1, H=1, d=1, rank=1, causal=True),
+    dict(B=3, Tq=17, Tkv=17, H=2, d=40, rank=100, causal=False),
+    dict(B=1, Tq=5, Tkv=70, H=4, d=33, rank=300, causal=True),
+])
+def test_warp_path_f32_shapes(oracle, shape):
+    w = custom_workload("odd", dtype="f32", **shape)
+    x = make_inputs(w, seed=7)
+    out = run_attention(x, w)
+    ref = oracle.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale, w.causal)
+    assert_f32_close(out, ref, str(shape))
+
+
+def test_projection_f32_odd(oracle):
+    g = torch.Generator().manual_seed(3)
+    h = torch.randn(17, 30, generator=g)
+    wd = torch.randn(30, 7, generator=g) / 5
+    wk = torch.randn(7, 10, generator=g) / 3
+    lat, k, v = mla.project(cuda(h), cuda(wd), cuda(wk), None)
+    rl, rk, _ = oracle.project(h, wd, wk, None)
+    assert v is None
+    assert_f32_close(lat, rl, "latent")
+    assert_f32_close(k, rk, "k")
+
+
+# ----------------------------------------------------------------- bf16 workloads
+def test_mid_bf16_full(oracle):
+    w = WORKLOADS["mid_bf16"]
+    x = make_inputs(w)
+    out = run_attention(x, w)
+    ref = explicit.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale)
+    assert_bf16_close(out, ref, "mid_bf16 vs explicit oracle")
+    rows = sample_rows(w.B, w.Tq, 4, seed=1)
+    lit = oracle.attention_rows(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale, rows)
+    got = to_np(out)[[r[0] for r in rows], [r[1] for r in rows]]
+    assert_bf16_close(got, lit, "mid_bf16 vs literal oracle rows")
+
+
+def test_prefill_bf16_attention_sampled(oracle):
+    w = WORKLOADS["prefill_bf16"]
+    x = make_inputs(w, with_projection=False)
+    out = run_attention(x, w)
+    assert torch.isfinite(out).all()
+    prep = oracle.prepare(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"])
+    rows = sample_rows(w.B, w.Tq, 8, seed=2, must=((0, 0), (1, 4095), (0, 127), (1, 128)))
+    ref = oracle.attention_rows(None, None, None, None, w.scale, rows, prepared=prep,
+                                form="absorbed")
+    got = to_np(out)[[r[0] for r in rows], [r[1] for r in rows]]
+    assert_bf16_close(got, ref, "prefill_bf16 sampled rows")
+    lit = oracle.attention_rows(None, None, None, None, w.scale, rows[:2], prepared=prep)
+    assert_bf16_close(got[:2], lit, "prefill_bf16 literal rows")
+
+
+def test_prefill_bf16_projection_chain(oracle):
+    """hidden -> latent (GPU, bf16) -> attention (GPU), against the oracle's
+    own float64 projection and attention of one sequence."""
+    w = WORKLOADS["prefill_bf16"]
+    x = make_inputs(w)
+    lat, _, _ = mla.project(cuda(x["hidden"]), cuda(x["w_down"]))
+    assert lat.dtype == torch.bfloat16 and lat.shape == (w.B, w.Tkv, w.rank)
+    b = 1
+    rl, _, _ = oracle.project(x["hidden"][b], x["w_down"])
+    assert_bf16_close(lat[b].float(), rl, "latent of sequence 1")
+    out = run_attention(x, w, lat=lat)
+    q1 = x["q"][b:b + 1]
+    rows = [(0, 0), (0, 1000), (0, 4095)]
+    ref = oracle.attention_rows(q1, rl.reshape(1, w.Tkv, w.rank), x["w_up_k"], x["w_up_v"],
+                                w.scale, rows, form="absorbed")
+    got = to_np(out)[b, [r[1] for r in rows]]
+    assert_bf16_close(got, ref, "projection -> attention chain")
+
+
+@pytest.mark.parametrize("splits", [0, 4])
+def test_decode_bf16_sampled(oracle, splits):
+    w = WORKLOADS["decode_bf16"]
+    x = make_inputs(w)
+    mla.set_option(_lib.OPT_KV_SPLITS, splits)
+    try:
+        out = run_attention(x, w)
+    finally:
+        mla.set_option(_lib.OPT_KV_SPLITS, 0)
+    prep = oracle.prepare(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"])
+    rows = [(0, 0), (17, 0), (63, 0)]
+    ref = oracle.attention_rows(None, None, None, None, w.scale, rows, prepared=prep,
+                                form="absorbed")
+    got = to_np(out)[[r[0] for r in rows], 0]
+    assert_bf16_close(got, ref, f"decode_bf16 splits={splits}")
+
+
+EDGE = [
+    dict(B=1, Tq=200, Tkv=200, H=3, d=64, rank=64, causal=True),       # ragged rows, small rank
+    dict(B=2, Tq=70, Tkv=300, H=5, d=128, rank=192, causal=True),      # chunked prefill
+    dict(B=1, Tq=130, Tkv=130, H=2, d=64, rank=384, causal=True),      # CTA pair, RC=192
+    dict(B=2, Tq=33, Tkv=100, H=4, d=64, rank=128, causal=False),      # no mask
+    dict(B=3, Tq=1, Tkv=1, H=1, d=64, rank=64, causal=True),           # a single key
+    dict(B=1, Tq=64, Tkv=64, H=2, d=192, rank=512, causal=True),       # pair, wide head
+]
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "x".join(str(v) for v in s.values()))
+@pytest.mark.parametrize("splits", [0, 3])
+def test_tensor_core_path_edges(oracle, shape, splits):
+    w = custom_workload("edge", dtype="bf16", **shape)
+    x = make_inputs(w, seed=11)
+    mla.set_option(_lib.OPT_KV_SPLITS, splits)
+    try:
+        assert mla.workspace_size(w.B, w.Tq, w.Tkv, w.H, w.d, w.rank, torch.bfloat16,
+                                  w.causal) > 0
+        out = run_attention(x, w)
+        outb = run_attention(x, w, out_dtype=torch.bfloat16)
+    finally:
+        mla.set_option(_lib.OPT_KV_SPLITS, 0)
+    ref = oracle.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale, w.causal)
+    assert_bf16_close(out, ref, f"{shape} splits={splits}")
+    assert_bf16_close(outb.float(), ref, f"{shape} splits={splits} bf16 out")
+
+
+def test_bf16_small_head_takes_warp_path(oracle):
+    w = custom_workload("small_bf16", dtype="bf16", B=2, Tq=40, Tkv=40, H=3, d=32, rank=48)
+    assert mla.workspace_size(w.B, w.Tq, w.Tkv, w.H, w.d, w.rank, torch.bfloat16) == 0
+    x = make_inputs(w, seed=5)
+    out = run_attention(x, w)
+    ref = oracle.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale)
+    assert_bf16_close(out, ref, "bf16 warp path")
+
+
+def test_projection_bf16_with_kv(oracle):
+    g = torch.Generator().manual_seed(9)
+    M, Dm, R, C = 200, 128, 64, 192
+    h = torch.randn(M, Dm, generator=g).bfloat16()
+    wd = (torch.randn(Dm, R, generator=g) / math.sqrt(Dm)).bfloat16()
+    wk = (torch.randn(R, C, generator=g) / 8).bfloat16()
+    wv = (torch.randn(R, C, generator=g) / 8).bfloat16()
+    lat, k, v = mla.project(cuda(h), cuda(wd), cuda(wk), cuda(wv))
+    rl, rk, rv = oracle.project(h, wd, wk, wv)
+    assert_bf16_close(lat.float(), rl, "latent")
+    assert_bf16_close(k.float(), rk, "k")
+    assert_bf16_close(v.float(), rv, "v")
+
+
+# ----------------------------------------------------------------- split-KV merge
+def test_merge_worked_example(oracle):
+    """Scores [-inf, 0, 0] as three one-key parts give (v1 + v2) / 2 (page
+    Kimi-K2.6 l2_p29's worked example), through mla_merge_partials."""
+    v = torch.tensor([[1.0, 2.0, -4.0, 9.0], [3.0, 5.0, 0.5, 1.0], [7.0, 11.0, -2.5, 3.0]])
+    m = torch.tensor([[-math.inf], [0.0], [0.0]])
+    l = torch.tensor([[0.0], [1.0], [1.0]])
+    o = (v * l).reshape(3, 1, 4)
+    out = mla.merge_partials(cuda(m), cuda(l), cuda(o))
+    np.testing.assert_array_equal(to_np(out)[0], (to_np(v[1]) + to_np(v[2])) / 2)
+
+
+def test_merge_random_against_oracle(oracle):
+    rng = np.random.default_rng(4)
+    parts, rows, width = 5, 37, 64
+    m = rng.standard_normal((parts, rows)) * 4
+    m[1, :5] = -np.inf                                   # empty parts
+    l = np.where(np.isinf(m), 0.0, rng.uniform(0.5, 3, (parts, rows)))
+    o = rng.standard_normal((parts, rows, width)) * l[..., None]
+    out = mla.merge_partials(cuda(torch.tensor(m, dtype=torch.float32)),
+                             cuda(torch.tensor(l, dtype=torch.float32)),
+                             cuda(torch.tensor(o, dtype=torch.float32)))
+    ln2 = math.log(2.0)
+    m32 = torch.tensor(m, dtype=torch.float32).double().numpy()
+    l32 = torch.tensor(l, dtype=torch.float32).double().numpy()
+    o32 = torch.tensor(o, dtype=torch.float32).double().numpy()
+    for r in range(rows):
+        ref = oracle.merge_partials(m32[:, r] * ln2, l32[:, r], o32[:, r])
+        assert_f32_close(to_np(out)[r], ref, f"row {r}")

@@ -126,6 +126,8 @@ def pin_last_queries(o):
     np.testing.assert_allclose(last, full[:, -3:], rtol=0, atol=1e-14)
     rows = o.attention_rows(q, lat, wk, wv, 0.6, [(0, 0), (1, 11), (0, 5)])
     np.testing.assert_allclose(rows, full[[0, 1, 0], [0, 11, 5]], rtol=0, atol=0)
+    rows_a = o.attention_rows(q, lat, wk, wv, 0.6, [(0, 0), (1, 11), (0, 5)], form="absorbed")
+    np.testing.assert_allclose(rows_a, rows, rtol=1e-12, atol=1e-13)
 
 
 def pin_projection(o):
