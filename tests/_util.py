@@ -2,8 +2,13 @@
 
 Tolerances (written out here, derived in the design notes):
   fp32 workloads: |gpu - ref| <= 1e-4 + 1e-4 * |ref| per element.
-  bf16 workloads: |gpu - ref| <= 2e-2 * |ref| + 2e-2 * rms(ref) per element,
-                  and ||gpu - ref||_2 <= 2e-2 * ||ref||_2 over the compared set.
+  bf16 workloads: the relative bound applies to each output row (the last
+                  axis: one head's d-vector, or one latent / k / v row):
+                  |gpu - ref| <= 2e-2 * |ref| + 2e-2 * rms(ref row) per element,
+                  ||gpu - ref row||_2 <= 2e-2 * ||ref row||_2 per row, and
+                  ||gpu - ref||_2 <= 2e-2 * ||ref||_2 over the compared set.
+                  (Rows at small t average few values and are several times
+                  larger than the global rms, so the scale is the row's own.)
 """
 import numpy as np
 import torch
@@ -29,10 +34,13 @@ def assert_f32_close(gpu, ref, what=""):
 def bf16_errors(gpu, ref):
     g, r = to_np(gpu), to_np(ref)
     err = np.abs(g - r)
-    rms = float(np.sqrt(np.mean(r * r)))
-    return dict(max_abs=float(err.max()), rms_ref=rms,
+    row_rms = np.sqrt(np.mean(r * r, axis=-1, keepdims=True))
+    row_norm = np.linalg.norm(r, axis=-1)
+    row_err = np.linalg.norm(g - r, axis=-1)
+    return dict(max_abs=float(err.max()),
                 normwise=float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-300)),
-                worst_ratio=float((err / (2e-2 * np.abs(r) + 2e-2 * rms)).max()))
+                worst_row=float((row_err / np.maximum(row_norm, 1e-300)).max()),
+                worst_ratio=float((err / (2e-2 * np.abs(r) + 2e-2 * row_rms + 1e-30)).max()))
 
 
 def assert_bf16_close(gpu, ref, what=""):
@@ -41,6 +49,7 @@ def assert_bf16_close(gpu, ref, what=""):
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     e = bf16_errors(g, r)
     assert e["worst_ratio"] <= 1.0, f"{what}: elementwise bound exceeded {e}"
+    assert e["worst_row"] <= 2e-2, f"{what}: row-relative error {e}"
     assert e["normwise"] <= 2e-2, f"{what}: normwise error {e}"
     return e
 
