@@ -1,0 +1,377 @@
+"""Benchmark of the latent causal attention path on GB300.
+
+One step = one pass of the whole path over the prefill workload
+(B=2, T=4096, H=32, d=128, rank=512, bf16): the down-projection
+latent = hidden @ w_down of hidden (2,4096,4096), then the causal latent
+attention on that latent (query absorption, flash loop over the latent,
+value up-projection).  The metric is algorithmic TFLOP/s of the step:
+  projection 2*M*model_dim*rank + attention 4*rank*pairs*H + 4*B*T*H*rank*d.
+A secondary line measures the bandwidth-bound decode workload (B=64, one
+query at t=4095, H=128) in GB/s of algorithmic bytes.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own copy of the workload (weak scaling, no
+collective on the data path); rank 0 prints one JSON line with the max time
+over ranks.  ``--impl reference`` times the float64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "latent-attention TFLOP/s and HBM GB/s on 1 GB300; fraction of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle timing
+_ORACLE_CACHE = {}
+
+
+def time_oracle(budget_s: float = 15.0, seed_rows: int = 0):
+    """The float64 oracle (its absorbed form, pinned equal to the literal
+    definition) over sampled (b, i) rows of the prefill workload, all heads;
+    returns (TFLOP/s of algorithmic work, details)."""
+    import numpy as np
+    import oracle
+    from latent_causal_attention_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS["prefill_bf16"]
+    if "prep" not in _ORACLE_CACHE:
+        x = make_inputs(w, with_projection=False)
+        _ORACLE_CACHE["o"] = oracle.get()
+        _ORACLE_CACHE["prep"] = _ORACLE_CACHE["o"].prepare(x["q"], x["kv_latent"], x["w_up_k"],
+                                                           x["w_up_v"])
+    o, prep = _ORACLE_CACHE["o"], _ORACLE_CACHE["prep"]
+    rng = np.random.default_rng(seed_rows)
+    cores = os.cpu_count() or 1
+    done_rows, flops, t_total = 0, 0.0, 0.0
+    while t_total < budget_s:
+        rows = [(int(rng.integers(w.B)), int(rng.integers(w.Tq))) for _ in range(cores)]
+        t0 = time.perf_counter()
+        o.attention_rows(None, None, None, None, w.scale, rows, prepared=prep, form="absorbed")
+        t_total += time.perf_counter() - t0
+        for (_, i) in rows:
+            flops += 4.0 * w.rank * (i + 1) * w.H + 4.0 * w.H * w.rank * w.d
+        done_rows += len(rows)
+    value = flops / t_total / 1e12
+    return value, {"kind": "oracle", "cores": cores,
+                   "sample": f"float64 C oracle (absorbed form, OpenMP over rows x heads), "
+                             f"{done_rows} random (b, i) rows x {w.H} heads of the prefill "
+                             f"attention B2 T4096 H32 d128 R512 in {t_total:.1f} s; algorithmic "
+                             f"FLOPs of those rows / wall time"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    steps = []
+    detail = None
+    for _ in range(args.warmup):
+        time_oracle(budget_s=0.5, seed_rows=123)
+    for k in range(args.steps):
+        v, detail = time_oracle(budget_s=max(1.0, 60.0 / max(args.steps, 1)), seed_rows=k)
+        steps.append(v)
+    value = statistics.mean(steps)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill_bf16: projection (2,4096,4096)@(4096,512) + causal "
+                                   "latent attention B2 T4096 H32 d128 rank512 (oracle: sampled "
+                                   "rows)", "l2": "n/a (CPU)"},
+            "cpu_baseline": {**detail, "value": round(value, 6), "unit": "TFLOP/s"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+
+    import latent_causal_attention_gb300 as mla
+    from latent_causal_attention_gb300.build import build
+    from latent_causal_attention_gb300.inputs import WORKLOADS, make_inputs
+
+    build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = load_peaks()
+
+    w = WORKLOADS["prefill_bf16"]
+    x = make_inputs(w)
+    d = {k: v.to(dev) for k, v in x.items()}
+    del d["kv_latent"]                        # the attention consumes the projection's latent
+    lat = torch.empty(w.B, w.Tkv, w.rank, device=dev, dtype=torch.bfloat16)
+    out = torch.empty(w.B, w.Tq, w.H, w.d, device=dev, dtype=torch.float32)
+    ws = torch.empty(max(1, mla.workspace_size(w.B, w.Tq, w.Tkv, w.H, w.d, w.rank,
+                                               torch.bfloat16)), device=dev, dtype=torch.uint8)
+    flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mla.project(d["hidden"], d["w_down"], latent=lat)
+        mla.attention(d["q"], lat, d["w_up_k"], d["w_up_v"], w.scale, True, out=out, workspace=ws)
+
+    flops_proj = w.projection_flops()
+    flops_attn = w.attention_flops()
+    flops_step = flops_proj + flops_attn
+    # algorithmic FLOPs of the flash kernel alone: q'.latent and p.latent over rank
+    flops_flash = 4 * w.rank * w.pairs() * w.H
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    ev = [mla.StageEvents() for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(int(vis.split(",")[local]) if vis else local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = mla.launch_count()
+    for k in range(args.steps):
+        flush.zero_()                          # L2 flush between timed steps (outside the events)
+        ev[k].install()
+        starts[k].record(stream)
+        step()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    mla.StageEvents.uninstall()
+    launches = mla.launch_count() - launches0
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    flash_ms = [e.elapsed_ms(1) for e in ev]
+    stages = {name: statistics.mean(e.elapsed_ms(i) for e in ev)
+              for i, name in [(4, "projection"), (0, "absorb"), (1, "flash"), (3, "v_up")]}
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+
+    # --- end to end: pinned host inputs -> device -> path -> host result
+    host = {k: v.pin_memory() for k, v in x.items() if k != "kv_latent"}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        for k_, v_ in host.items():
+            d[k_].copy_(v_, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = es.elapsed_time(ee)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    # --- decode workload (bandwidth-bound): GB/s of algorithmic bytes
+    dec = None
+    if not args.no_decode:
+        wd = WORKLOADS["decode_bf16"]
+        xd = {k: v.to(dev) for k, v in make_inputs(wd).items()}
+        outd = torch.empty(wd.B, wd.Tq, wd.H, wd.d, device=dev, dtype=torch.float32)
+        wsd = torch.empty(max(1, mla.workspace_size(wd.B, wd.Tq, wd.Tkv, wd.H, wd.d, wd.rank,
+                                                    torch.bfloat16)), device=dev,
+                          dtype=torch.uint8)
+
+        def dstep():
+            mla.attention(xd["q"], xd["kv_latent"], xd["w_up_k"], xd["w_up_v"], wd.scale, True,
+                          out=outd, workspace=wsd)
+
+        for _ in range(max(3, args.warmup)):
+            dstep()
+        n = max(10, args.steps)
+        dev_ev = [mla.StageEvents() for _ in range(n)]
+        s_ = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        e_ = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        torch.cuda.synchronize()
+        for k in range(n):
+            flush.zero_()
+            dev_ev[k].install()
+            s_[k].record(stream)
+            dstep()
+            e_[k].record(stream)
+        torch.cuda.synchronize()
+        mla.StageEvents.uninstall()
+        dms = statistics.mean(a.elapsed_time(b) for a, b in zip(s_, e_))
+        dflash = statistics.mean(e.elapsed_ms(1) for e in dev_ev)
+        nbytes = wd.attention_bytes(out_bytes=4)
+        dec = {"workload": "decode_bf16: B64, one query at t=4095 over 4096 latent rows, H128 d128 "
+                           "rank512, bf16 in, fp32 out",
+               "GB_per_s": round(nbytes / (dms * 1e-3) / 1e9, 1),
+               "ms": round(dms, 4), "algorithmic_bytes": nbytes,
+               "frac_hbm": round(nbytes / (dms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+               "TFLOP_per_s": round(wd.attention_flops() / (dms * 1e-3) / 1e12, 2),
+               "flash_ms": round(dflash, 4),
+               "flash_frac_hbm": round(268435456 * 1.0 / (dflash * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                       4)}
+
+    if rank != 0:
+        return
+    flash_avg = statistics.mean(flash_ms)
+    achieved = flops_flash / (flash_avg * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    cpu_val, cpu_detail = (None, None)
+    if not args.no_cpu_baseline:
+        cpu_val, cpu_detail = time_oracle(budget_s=15.0)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0, std) inputs of the workload's shapes)",
+        "config": {"workload": "prefill_bf16: projection hidden (2,4096,4096) @ w_down (4096,512) "
+                               "-> bf16 latent, then causal latent attention B2 T4096 H32 d128 "
+                               "rank512, fp32 out",
+                   "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                   "flops_per_step": flops_step},
+        "stages_ms": {k: round(v, 4) for k, v in stages.items()},
+        "frac_of_peak_step": round(value / world / peak, 4),
+        "roofline": {"bound": "tensor", "kernel": "flash_packed_kernel",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                     "flops_per_launch": flops_flash, "traffic": None},
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "decode": dec,
+    }
+    if cpu_val is not None:
+        line["cpu_baseline"] = {**cpu_detail, "value": round(cpu_val, 6), "unit": "TFLOP/s"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

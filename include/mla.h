@@ -160,6 +160,22 @@ typedef enum {
 } mla_option_t;
 mla_status_t mla_set_option(int option, int64_t value);
 
+/*
+ * Profiling hook.  When events != NULL, every later mla_latent_attention and
+ * mla_kv_latent_project call records events[2*s] just before and
+ * events[2*s+1] just after its stage s, on the call's stream:
+ *   s = 0 query absorption GEMM, 1 flash loop, 2 split-KV merge,
+ *   3 value up-projection GEMM, 4 projection GEMM (hidden @ w_down),
+ *   5 projection k / v GEMMs.
+ * n is the number of cudaEvent_t handles in the array; stages with
+ * 2*s+1 >= n are not recorded.  The caller creates, owns and destroys the
+ * events (created with timing enabled).  NULL disables recording.
+ */
+mla_status_t mla_set_stage_events(void** events, int n);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t mla_launch_count(void);
+
 /* Human-readable name of a status code (static string). */
 const char* mla_status_string(int status);
 

@@ -19,7 +19,8 @@ from . import _lib
 from ._lib import MLAError, MLA_BF16, MLA_F32
 
 __all__ = ["project", "attention", "attention_from_host", "workspace_size", "merge_partials",
-           "set_option", "device_error", "MLAError", "dtype_code"]
+           "set_option", "device_error", "launch_count", "StageEvents", "MLAError",
+           "dtype_code"]
 
 
 def dtype_code(dt: torch.dtype) -> int:
@@ -147,6 +148,37 @@ def merge_partials(m: torch.Tensor, l: torch.Tensor, o: torch.Tensor,
 
 def set_option(option: int, value: int) -> None:
     _lib.check("mla_set_option", _lib.load().mla_set_option(option, value))
+
+
+class StageEvents:
+    """Per-stage CUDA events recorded by the library around its kernels (see
+    mla_set_stage_events).  Stages: 0 absorb, 1 flash, 2 merge, 3 value
+    up-projection, 4 projection, 5 projection k/v."""
+
+    NSTAGE = 6
+
+    def __init__(self):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * self.NSTAGE)]
+        for e in self.events:          # create the underlying cudaEvent_t now
+            e.record()
+        torch.cuda.synchronize()
+        self._arr = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        self.used = set()
+
+    def install(self) -> None:
+        _lib.check("mla_set_stage_events",
+                   _lib.load().mla_set_stage_events(self._arr, len(self.events)))
+
+    @staticmethod
+    def uninstall() -> None:
+        _lib.load().mla_set_stage_events(None, 0)
+
+    def elapsed_ms(self, stage: int) -> float:
+        return self.events[2 * stage].elapsed_time(self.events[2 * stage + 1])
+
+
+def launch_count() -> int:
+    return int(_lib.load().mla_launch_count())
 
 
 def device_error(clear: bool = False) -> int:

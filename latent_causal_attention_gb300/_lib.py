@@ -28,6 +28,8 @@ SIGNATURES = {
     "mla_get_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
     "mla_set_option": (_i, [_i, _i64]),
     "mla_status_string": (ctypes.c_char_p, [_i]),
+    "mla_set_stage_events": (_i, [ctypes.POINTER(ctypes.c_void_p), _i]),
+    "mla_launch_count": (ctypes.c_uint64, []),
 }
 
 

@@ -58,6 +58,26 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t d
 // ---------------------------------------------------------------------------
 static int g_attn_path = 0;     // 0 auto, 1 warp, 2 tensor core
 static int g_kv_splits = 0;     // 0 auto
+static void** g_stage_events = nullptr;
+static int g_stage_events_n = 0;
+static unsigned long long g_launches = 0;
+
+// Records the "before" (edge 0) or "after" (edge 1) event of a stage.
+static void stage_event(int stage, int edge, cudaStream_t stream) {
+  const int i = 2 * stage + edge;
+  if (g_stage_events && i < g_stage_events_n && g_stage_events[i])
+    cudaEventRecord(static_cast<cudaEvent_t>(g_stage_events[i]), stream);
+}
+
+// Wraps one kernel launch: stage events around it and the launch counter.
+template <typename F>
+static cudaError_t staged(int stage, cudaStream_t stream, F&& launch) {
+  stage_event(stage, 0, stream);
+  cudaError_t e = launch();
+  stage_event(stage, 1, stream);
+  if (e == cudaSuccess) __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  return e;
+}
 
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -158,6 +178,15 @@ mla_status_t mla_set_option(int option, int64_t value) {
   }
 }
 
+mla_status_t mla_set_stage_events(void** events, int n) {
+  if (events != nullptr && n <= 0) return MLA_ERR_SHAPE;
+  g_stage_events = events;
+  g_stage_events_n = events ? n : 0;
+  return MLA_OK;
+}
+
+uint64_t mla_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
 mla_status_t mla_get_device_error(unsigned int* code, int clear) {
   if (!code) return MLA_ERR_NULL;
   unsigned int a = 0, b = 0;
@@ -192,10 +221,11 @@ mla_status_t mla_kv_latent_project(const void* hidden, const void* w_down, const
                   (!v || (aligned16(v) && aligned16(w_up_v)));
   if (!tc) {
     if (rank > 512) return MLA_ERR_UNSUPPORTED;
-    return cuda_status(launch_projection_cuda_core(hidden, w_down, w_up_k, w_up_v, latent, k, v, M,
-                                                   model_dim, rank, want_kv ? kv_dim : 0,
-                                                   in_dtype == MLA_BF16, out_dtype == MLA_BF16,
-                                                   stream));
+    return cuda_status(staged(4, stream, [&] {
+      return launch_projection_cuda_core(hidden, w_down, w_up_k, w_up_v, latent, k, v, M,
+                                         model_dim, rank, want_kv ? kv_dim : 0,
+                                         in_dtype == MLA_BF16, out_dtype == MLA_BF16, stream);
+    }));
   }
   // Stage 1: latent = hidden @ w_down  (A K-major, B = w_down MN-major).
   CUtensorMap mA, mB;
@@ -208,7 +238,7 @@ mla_status_t mla_kv_latent_project(const void* hidden, const void* w_down, const
   GemmArgs g = {};
   g.M = (int)M; g.N = rank; g.K = model_dim; g.G = 1; g.BN = pick_bn(rank); g.alpha = 1.f;
   g.C = latent; g.c_bf16 = out_dtype == MLA_BF16; g.c_rs = rank; g.c_gs = 0;
-  cudaError_t e = launch_gemm_tc(mA, mB, true, g, stream);
+  cudaError_t e = staged(4, stream, [&] { return launch_gemm_tc(mA, mB, true, g, stream); });
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (!want_kv) return MLA_OK;
   // Stage 2: k / v = latent(bf16) @ w_up_k / w_up_v.
@@ -227,7 +257,7 @@ mla_status_t mla_kv_latent_project(const void* hidden, const void* w_down, const
     GemmArgs g2 = {};
     g2.M = (int)M; g2.N = kv_dim; g2.K = rank; g2.G = 1; g2.BN = pick_bn(kv_dim); g2.alpha = 1.f;
     g2.C = outs[i]; g2.c_bf16 = 1; g2.c_rs = kv_dim; g2.c_gs = 0;
-    e = launch_gemm_tc(mL, mW, true, g2, stream);
+    e = staged(5, stream, [&] { return launch_gemm_tc(mL, mW, true, g2, stream); });
     if (e != cudaSuccess) return MLA_ERR_CUDA;
   }
   return MLA_OK;
@@ -265,9 +295,11 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
   if (!p.tc) {
     if (g_attn_path == 2) return MLA_ERR_UNSUPPORTED;
     if (rank > 1024 || d > 256) return MLA_ERR_UNSUPPORTED;
-    return cuda_status(launch_warp_attention(q, kv_latent, w_up_k, w_up_v, out, B, Tq, Tkv, H, d,
-                                             rank, scale, causal, in_dtype == MLA_BF16,
-                                             out_dtype == MLA_BF16, stream));
+    return cuda_status(staged(1, stream, [&] {
+      return launch_warp_attention(q, kv_latent, w_up_k, w_up_v, out, B, Tq, Tkv, H, d, rank,
+                                   scale, causal, in_dtype == MLA_BF16, out_dtype == MLA_BF16,
+                                   stream);
+    }));
   }
   if (!workspace) return MLA_ERR_WORKSPACE;
   if (workspace_bytes < p.total) return MLA_ERR_WORKSPACE;
@@ -291,7 +323,8 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
   g.M = (int)BT; g.N = R; g.K = d; g.G = H; g.BN = bn_abs;
   g.alpha = scale * 1.4426950408889634f;
   g.C = qp; g.c_bf16 = 1; g.c_rs = (int64_t)H * R; g.c_gs = R;
-  if (launch_gemm_tc(mA, mB, false, g, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (staged(0, stream, [&] { return launch_gemm_tc(mA, mB, false, g, stream); }) != cudaSuccess)
+    return MLA_ERR_CUDA;
 
   // 2. flash loop over the latent
   CUtensorMap mQ, mL;
@@ -307,12 +340,15 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
   fa.olat = olat;
   fa.part_o = p.splits > 1 ? reinterpret_cast<float*>(ws + p.off_po) : nullptr;
   fa.part_ml = p.splits > 1 ? reinterpret_cast<float*>(ws + p.off_pml) : nullptr;
-  if (launch_flash_packed(mQ, mL, fa, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (staged(1, stream, [&] { return launch_flash_packed(mQ, mL, fa, stream); }) != cudaSuccess)
+    return MLA_ERR_CUDA;
 
   // 3. merge the key-range partitions
   if (p.splits > 1) {
-    if (launch_merge_partials(fa.part_ml, 2, nullptr, fa.part_o, olat, p.splits, (int)p.rows, R, 1,
-                              stream) != cudaSuccess)
+    if (staged(2, stream, [&] {
+          return launch_merge_partials(fa.part_ml, 2, nullptr, fa.part_o, olat, p.splits,
+                                       (int)p.rows, R, 1, stream);
+        }) != cudaSuccess)
       return MLA_ERR_CUDA;
   }
 
@@ -326,7 +362,8 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
   GemmArgs g2 = {};
   g2.M = (int)BT; g2.N = d; g2.K = R; g2.G = H; g2.BN = pick_bn(d); g2.alpha = 1.f;
   g2.C = out; g2.c_bf16 = out_dtype == MLA_BF16; g2.c_rs = (int64_t)H * d; g2.c_gs = d;
-  if (launch_gemm_tc(mO, mV, true, g2, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (staged(3, stream, [&] { return launch_gemm_tc(mO, mV, true, g2, stream); }) != cudaSuccess)
+    return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
@@ -336,9 +373,11 @@ mla_status_t mla_merge_partials(const float* m, const float* l, const float* o, 
   if (parts <= 0 || rows <= 0 || width <= 0 || width % 4 != 0) return MLA_ERR_SHAPE;
   if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
   if (!aligned16(o) || !aligned16(out)) return MLA_ERR_ALIGN;
-  return cuda_status(launch_merge_partials(m, 1, l, o, out, parts, rows, width,
-                                           out_dtype == MLA_BF16,
-                                           static_cast<cudaStream_t>(stream_)));
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  return cuda_status(staged(2, stream, [&] {
+    return launch_merge_partials(m, 1, l, o, out, parts, rows, width, out_dtype == MLA_BF16,
+                                 stream);
+  }));
 }
 
 }  // extern "C"
