@@ -129,6 +129,41 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
                                   void* stream);
 
 /*
+ * Allocation-free variant of mla_latent_attention (no counterpart on the
+ * pages; it exists for callers, not for the method).
+ *
+ * Some callers cannot allocate device memory at the point where they run
+ * attention: code that must not call cudaMalloc / cudaFree on its hot path
+ * (they synchronise the device), plugins that run inside a host framework
+ * owning all GPU memory, or runtimes with a fixed memory budget.  This call
+ * takes the same inputs and output as mla_latent_attention but no workspace:
+ * its scratch is a fixed array of MLA_NOALLOC_SCRATCH_BYTES bytes that lives
+ * in the library's device memory on every GPU that loads the library, for as
+ * long as the process runs.
+ *
+ *   - Returns MLA_ERR_WORKSPACE (nothing launched) when the scratch these
+ *     sizes need, mla_latent_attention_workspace_size(...), exceeds
+ *     MLA_NOALLOC_SCRATCH_BYTES.  The warp-per-query path needs none.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.  Later calls only reuse the address.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents (nothing in it has to start at zero: every byte read is
+ *     written earlier in the same call).  Calls whose kernels overlap on the
+ *     GPU (different streams, or different host threads) race on it; issue
+ *     them on one stream, or use mla_latent_attention with your own
+ *     workspace.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ * Other arguments, results and errors as mla_latent_attention.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+mla_status_t mla_latent_attention_noalloc(const void* q, const void* kv_latent,
+                                          const void* w_up_k, const void* w_up_v, void* out,
+                                          int B, int Tq, int Tkv, int H, int d, int rank,
+                                          float scale, int causal, int in_dtype, int out_dtype,
+                                          void* stream);
+
+/*
  * Split-KV merge (the online-softmax merge of partial states; page
  * "Kimi-K2.6 l2_p29", online softmax with running max and rescaling by
  * exp(m - m_new), -inf handling): for each row r and part p < parts,

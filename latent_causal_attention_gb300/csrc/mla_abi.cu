@@ -381,3 +381,52 @@ mla_status_t mla_merge_partials(const float* m, const float* l, const float* o, 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free attention: the scratch is this file's device array.
+// ---------------------------------------------------------------------------
+namespace mla {
+
+// Device scratch of mla_latent_attention_noalloc, one copy per GPU that loads
+// the library.  In host code this name is only a stand-in for the symbol: its
+// device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device.
+static cudaError_t noalloc_scratch(void** addr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace mla
+
+extern "C" mla_status_t mla_latent_attention_noalloc(const void* q, const void* kv_latent,
+                                                     const void* w_up_k, const void* w_up_v,
+                                                     void* out, int B, int Tq, int Tkv, int H,
+                                                     int d, int rank, float scale, int causal,
+                                                     int in_dtype, int out_dtype, void* stream) {
+  const size_t need =
+      mla_latent_attention_workspace_size(B, Tq, Tkv, H, d, rank, in_dtype, causal);
+  if (need > (size_t)MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (need > 0 && mla::noalloc_scratch(&scratch) != cudaSuccess) return MLA_ERR_CUDA;
+  return mla_latent_attention(q, kv_latent, w_up_k, w_up_v, out, B, Tq, Tkv, H, d, rank, scale,
+                              causal, in_dtype, out_dtype, scratch,
+                              need > 0 ? (size_t)MLA_NOALLOC_SCRATCH_BYTES : 0, stream);
+}
