@@ -15,20 +15,24 @@
 // no visible key yet keeps m = -inf without producing NaN.
 //
 // Tile: 128 rows (query position, head) x 64 keys.  The latent tile in shared
-// memory (128-byte swizzle, rank-contiguous rows) feeds both MMAs: K-major as
-// the B operand of S = q' L^T and MN-major as the B operand of O += P L.
-// O_lat (128 x rank fp32) lives in tensor memory.  A 512-wide rank would fill
-// all 512 TMEM columns, so for rank > 256 two CTAs of a cluster split the
-// rank: each holds q', the latent tiles and O_lat for its half, computes a
-// partial S over its half, and the pair exchanges the partial S tiles through
-// distributed shared memory; both then run the identical softmax (the sum of
-// the two partials is the same bits in either CTA) and accumulate their half
-// of O_lat.
+// memory (128-byte swizzle, rank-contiguous rows) is the B operand of both
+// MMAs: K-major for S = q' L^T and MN-major for O += P L.  q' (bf16) sits in
+// tensor memory as the A operand of S, so S reads only the latent tile from
+// shared memory.  Tensor memory (512 columns x 128 lanes of 32 bits):
+//   [0, RC)      O_lat, fp32         [256, 384)  two 64-column S buffers
+//   [384, 512)   q', bf16 pairs (RC/2 columns)
+// A 512-wide rank cannot keep O_lat next to S, so for rank > 256 two CTAs of a
+// cluster split the rank: each holds q', the latent tiles and O_lat for its
+// half and computes a partial S over its half; dedicated exchange warps send
+// each partial S tile to the peer through distributed shared memory one step
+// ahead of the softmax (double-buffered receive buffers).  Both CTAs then run
+// the identical softmax (a + b is the same bits in either CTA) and accumulate
+// their half of O_lat.
 //
-// Warp roles (192 threads): warp 0 lane 0 = TMA producer (q' once, then a
-// 3-stage ring of latent tiles); warp 1 = TMEM owner, lane 0 issues MMAs;
-// warps 2-5 = softmax, one thread per row (warp w reads TMEM lanes
-// 32*(w%4)..+31), and the epilogue.
+// Warp roles (320 threads): warp 0 lane 0 = TMA producer (q' once, then a
+// 4-stage ring of latent tiles); warp 1 = TMEM owner, lane 0 issues MMAs;
+// warps 2-5 = partial-S exchange (CTA pair only); warps 6-9 = softmax, one
+// thread per row, and the epilogue.  Warp w reads TMEM lanes 32*(w%4)..+31.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -41,36 +45,36 @@ namespace {
 
 constexpr int kRows = 128;           // rows per CTA tile (MMA M)
 constexpr int kKeys = 64;            // keys per tile (S MMA N, O MMA K)
-constexpr int kStages = 3;           // latent tile ring
+constexpr int kStages = 4;           // latent tile ring
 constexpr int kMaxRC = 256;          // rank columns per CTA
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
 
-constexpr int kQBytes = kRows * kMaxRC * 2;       // 64 KB
 constexpr int kLStage = kKeys * kMaxRC * 2;       // 32 KB
 constexpr int kPBytes = kRows * kKeys * 2;        // 16 KB
-constexpr int kXBytes = kRows * kKeys * 4;        // 32 KB
-constexpr int kOffQ = 0;
-constexpr int kOffL = kOffQ + kQBytes;
+constexpr int kXBytes = kRows * kKeys * 4;        // 32 KB per receive buffer
+constexpr int kOffL = 0;
 constexpr int kOffP = kOffL + kStages * kLStage;
-constexpr int kOffX = kOffP + 2 * kPBytes;
-constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kOffX = kOffP + 2 * kPBytes;        // also the staging area of q' (64 KB)
+constexpr int kOffBar = kOffX + 2 * kXBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;   // + barriers + alignment slack
 
 constexpr uint32_t kTmemO = 0;       // columns [0, RC)
 constexpr uint32_t kTmemS = 256;     // two 64-column S buffers at 256, 320
+constexpr uint32_t kTmemQ = 384;     // q' as bf16 pairs, RC/2 columns
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full;             // q' staged in shared memory (TMA)
+  uint64_t q_ready;            // q' copied into tensor memory (softmax threads)
   uint64_t l_full[kStages];
   uint64_t l_empty[kStages];
   uint64_t s_full[2];
-  uint64_t s_empty[2];
+  uint64_t s_empty[2];         // softmax threads (+ exchange threads in a pair)
   uint64_t p_full[2];
   uint64_t p_empty[2];
   uint64_t o_last;
-  uint64_t x_full;     // my exchange buffer was filled by the peer
-  uint64_t x_empty;    // the peer's exchange buffer may be written again
+  uint64_t x_full[2];          // my receive buffer b was filled by the peer
+  uint64_t x_empty[2];         // the peer's receive buffer b may be written again
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -90,11 +94,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int si
   return __all_sync(0xffffffffu, ok);
 }
 
-// Position of 16-byte chunk c (0..15) of row r in the 256-byte rows of the
-// exchange buffer; the low three chunk bits are XOR-ed with the row so that
+// Position of 16-byte chunk c (0..15) of row r in the 256-byte rows of a
+// receive buffer; the low three chunk bits are XOR-ed with the row so that
 // eight consecutive rows hit eight different bank groups.
 __device__ __forceinline__ uint32_t x_offset(uint32_t r, uint32_t c) {
   return r * 256u + (((c & 8u) | ((c ^ r) & 7u)) << 4);
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&s)[64]) {
+  float(&a0)[32] = *reinterpret_cast<float(*)[32]>(&s[0]);
+  float(&a1)[32] = *reinterpret_cast<float(*)[32]>(&s[32]);
+  tmem_ld32(taddr, a0);
+  tmem_ld32(taddr + 32, a1);
+  tmem_wait_ld();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -103,7 +115,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t flash_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(flash_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + kOffQ;
   uint8_t* sL = smem + kOffL;
   uint8_t* sP = smem + kOffP;
   uint8_t* sX = smem + kOffX;
@@ -136,19 +147,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_ready, 128);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->l_full[s], 1);
       mbar_init(&bars->l_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], 128);
+      mbar_init(&bars->s_empty[i], a.pair ? 256 : 128);
       mbar_init(&bars->p_full[i], 128);
       mbar_init(&bars->p_empty[i], 1);
+      mbar_init(&bars->x_full[i], 128);
+      mbar_init(&bars->x_empty[i], 128);
     }
     mbar_init(&bars->o_last, 1);
-    mbar_init(&bars->x_full, 128);
-    mbar_init(&bars->x_empty, 128);
     bars->abort_flag = 0;
     fence_mbarrier_init_cluster();
   }
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&mapL);
       mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
       for (int kc = 0; kc < nchunk; ++kc)
-        tma_load_3d(sQ + kc * (kRows * 128), &mapQ, &bars->q_full, c0 + 64 * kc, row0, b);
+        tma_load_3d(sX + kc * (kRows * 128), &mapQ, &bars->q_full, c0 + 64 * kc, row0, b);
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int st = j % kStages;
@@ -188,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && nt > 0) {
       const uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
       const uint32_t idesc_o = make_idesc_bf16(kRows, RC, false, true);
-      const uint32_t q0 = smem_u32(sQ), l0 = smem_u32(sL), p0 = smem_u32(sP);
-      bool ok = mbar_wait(&bars->q_full, 0, 20, abort_flag);
+      const uint32_t l0 = smem_u32(sL), p0 = smem_u32(sP);
+      bool ok = mbar_wait(&bars->q_ready, 0, 20, abort_flag);
+      tc_fence_after();
       auto issue_o = [&](int jj) -> bool {
         if (!mbar_wait(&bars->p_full[jj & 1], (jj >> 1) & 1, 21, abort_flag)) return false;
         tc_fence_after();
@@ -213,16 +226,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lst = l0 + st * kLStage;
         const uint32_t sbuf = tmem + kTmemS + (j & 1) * kKeys;
         for (int k = 0; k < RC / 16; ++k) {
-          const uint32_t kc = k >> 2, kw = k & 3;
-          const uint64_t ad = make_sdesc_sw128(q0 + kc * (kRows * 128) + kw * 32, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(lst + kc * (kKeys * 128) + kw * 32, 16, 1024);
-          umma_bf16(sbuf, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          const uint64_t bd = make_sdesc_sw128(lst + (k >> 2) * (kKeys * 128) + (k & 3) * 32, 16,
+                                               1024);
+          umma_bf16_ta(sbuf, tmem + kTmemQ + k * 8, bd, idesc_s, k > 0 ? 1u : 0u);
         }
         umma_commit(&bars->s_full[j & 1]);
         if (j > 0 && !issue_o(j - 1)) { ok = false; break; }
       }
       if (ok) issue_o(nt - 1);
       umma_commit(&bars->o_last);
+    }
+  } else if (warp < 6) {
+    // ======================= partial-S exchange (CTA pair) =======================
+    if (a.pair && nt > 0) {
+      const int qd = warp & 3;
+      const uint32_t r = (uint32_t)(qd * 32 + lane);
+      const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+      const uint32_t x_peer0 = mapa_shared(smem_u32(sX), peer);
+      const uint32_t xfull_peer0 = mapa_shared(smem_u32(&bars->x_full[0]), peer);
+      const uint32_t xfull_peer1 = mapa_shared(smem_u32(&bars->x_full[1]), peer);
+      for (int j = 0; j < nt; ++j) {
+        const int bi = j & 1, k = j >> 1;
+        if (!warp_wait(&bars->s_full[bi], k & 1, 40, abort_flag)) break;
+        tc_fence_after();
+        float v[64];
+        tmem_ld64(tmem + lane_base + kTmemS + bi * kKeys, v);
+        tc_fence_before();
+        mbar_arrive(&bars->s_empty[bi]);
+        if (!warp_wait<true>(&bars->x_empty[bi], k & 1, 41, abort_flag)) break;
+        const uint32_t dst = x_peer0 + bi * kXBytes;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_cluster_v4(dst + x_offset(r, c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        mbar_arrive_remote(bi ? xfull_peer1 : xfull_peer0);
+      }
     }
   } else {
     // ======================= softmax / epilogue =======================
@@ -233,58 +270,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_row = a.Tkv - a.Tq + (row_valid ? grow / a.H : 0);
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const uint32_t x_local = smem_u32(sX);
-    const uint32_t x_peer = a.pair ? mapa_shared(x_local, peer) : 0u;
-    const uint32_t xfull_peer = a.pair ? mapa_shared(smem_u32(&bars->x_full), peer) : 0u;
-    const uint32_t xempty_peer = a.pair ? mapa_shared(smem_u32(&bars->x_empty), peer) : 0u;
+    const uint32_t xempty_peer0 = a.pair ? mapa_shared(smem_u32(&bars->x_empty[0]), peer) : 0u;
+    const uint32_t xempty_peer1 = a.pair ? mapa_shared(smem_u32(&bars->x_empty[1]), peer) : 0u;
 
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nt && ok; ++j) {
-      float s[kKeys];
-      if (!warp_wait(&bars->s_full[j & 1], (j >> 1) & 1, 30, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      {
-        float* s0 = s;
-        float(&a0)[32] = *reinterpret_cast<float(*)[32]>(s0);
-        float(&a1)[32] = *reinterpret_cast<float(*)[32]>(s0 + 32);
-        const uint32_t sb = tmem + lane_base + kTmemS + (j & 1) * kKeys;
-        tmem_ld32(sb, a0);
-        tmem_ld32(sb + 32, a1);
-        tmem_wait_ld();
+    bool ok = nt > 0;
+    if (ok) {
+      // q' (staged by TMA in the receive buffers, 128-byte swizzled rows) -> TMEM
+      ok = warp_wait(&bars->q_full, 0, 29, abort_flag);
+      if (ok) {
+        const uint32_t qs = x_local;
+        for (int kc = 0; kc < nchunk; ++kc) {
+          uint32_t u[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t addr = qs + kc * (kRows * 128) + sw128_offset((uint32_t)r, (uint32_t)c);
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(u[4 * c]), "=r"(u[4 * c + 1]), "=r"(u[4 * c + 2]),
+                           "=r"(u[4 * c + 3])
+                         : "r"(addr)
+                         : "memory");
+          }
+          tmem_st32u(tmem + lane_base + kTmemQ + kc * 32, u);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->q_ready);
+        if (a.pair) {                 // my receive buffers may now be written by the peer
+          mbar_arrive_remote(xempty_peer0);
+          mbar_arrive_remote(xempty_peer1);
+        }
       }
-      tc_fence_before();
-      mbar_arrive(&bars->s_empty[j & 1]);
+    }
+    for (int j = 0; j < nt && ok; ++j) {
+      const int bi = j & 1, k = j >> 1;
+      float s[kKeys];
+      if (!warp_wait(&bars->s_full[bi], k & 1, 30, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      tmem_ld64(tmem + lane_base + kTmemS + bi * kKeys, s);
 
       if (a.pair) {
-        // partial S over my half of the rank -> peer; peer's partial -> mine
-        if (!warp_wait<true>(&bars->x_empty, (j & 1) ^ 1, 31, abort_flag)) { ok = false; break; }
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_cluster_v4(x_peer + x_offset(r, c), s[4 * c], s[4 * c + 1], s[4 * c + 2],
-                        s[4 * c + 3]);
-        mbar_arrive_remote(xfull_peer);
-        if (!warp_wait<true>(&bars->x_full, j & 1, 32, abort_flag)) { ok = false; break; }
+        // the peer's partial S over its half of the rank
+        if (!warp_wait<true>(&bars->x_full[bi], k & 1, 32, abort_flag)) { ok = false; break; }
+        const uint32_t src = x_local + bi * kXBytes;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           float x0, x1, x2, x3;
-          ld_shared_v4f(x_local + x_offset(r, c), x0, x1, x2, x3);
+          ld_shared_v4f(src + x_offset(r, c), x0, x1, x2, x3);
           s[4 * c] += x0;
           s[4 * c + 1] += x1;
           s[4 * c + 2] += x2;
           s[4 * c + 3] += x3;
         }
-        mbar_arrive_remote(xempty_peer);
+        mbar_arrive_remote(bi ? xempty_peer1 : xempty_peer0);
       }
+      tc_fence_before();
+      mbar_arrive(&bars->s_empty[bi]);
 
       // mask: key s_idx visible iff s_idx < Tkv and (not causal or s_idx <= t)
       const int key0 = (tile0 + j) * kKeys;
       const int lim = a.causal ? min(t_row + 1, a.Tkv) : a.Tkv;   // visible keys < lim
       float mx = -INFINITY;
+      if (!row_valid || key0 + kKeys > lim) {
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        if (!row_valid || key0 + c >= lim) s[c] = -INFINITY;
-        mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < kKeys; ++c)
+          if (!row_valid || key0 + c >= lim) s[c] = -INFINITY;
       }
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) mx = fmaxf(mx, s[c]);
       const float m_new = fmaxf(m_run, mx);
       const bool grow_max = m_new > m_run + kRescaleThreshold;   // false while both -inf
       const float m_ref = grow_max ? m_new : m_run;
@@ -318,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // P (bf16) into the K-major swizzled P buffer
-      if (!warp_wait(&bars->p_empty[j & 1], ((j >> 1) & 1) ^ 1, 34, abort_flag)) { ok = false; break; }
-      const uint32_t pb = smem_u32(sP + (j & 1) * kPBytes);
+      if (!warp_wait(&bars->p_empty[bi], (k & 1) ^ 1, 34, abort_flag)) { ok = false; break; }
+      const uint32_t pb = smem_u32(sP + bi * kPBytes);
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         st_shared_v4(pb + sw128_offset(r, c), pack_bf16x2(s[8 * c], s[8 * c + 1]),
@@ -328,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[j & 1]);
+      mbar_arrive(&bars->p_full[bi]);
     }
 
     // ---------------- epilogue ----------------
@@ -337,7 +390,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool have_o = false;
     if (ok && nt > 0) {
       have_o = warp_wait(&bars->o_last, 0, 35, abort_flag);
-      __syncwarp();
       tc_fence_after();
     }
     if (a.splits == 1) {
