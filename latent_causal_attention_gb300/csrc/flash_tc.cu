@@ -29,10 +29,11 @@
 // the identical softmax (a + b is the same bits in either CTA) and accumulate
 // their half of O_lat.
 //
-// Warp roles (320 threads): warp 0 lane 0 = TMA producer (q' once, then a
+// Warp roles (448 threads): warp 0 lane 0 = TMA producer (q' once, then a
 // 4-stage ring of latent tiles); warp 1 = TMEM owner, lane 0 issues MMAs;
-// warps 2-5 = partial-S exchange (CTA pair only); warps 6-9 = softmax, one
-// thread per row, and the epilogue.  Warp w reads TMEM lanes 32*(w%4)..+31.
+// warps 2-5 = partial-S exchange (CTA pair only); warps 6-13 = softmax and
+// epilogue, two warps per row quadrant (each takes 32 of a tile's 64 keys and
+// half of O_lat's columns).  Warp w reads TMEM lanes 32*(w%4)..+31.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -47,7 +48,7 @@ constexpr int kRows = 128;           // rows per CTA tile (MMA M)
 constexpr int kKeys = 64;            // keys per tile (S MMA N, O MMA K)
 constexpr int kStages = 4;           // latent tile ring
 constexpr int kMaxRC = 256;          // rank columns per CTA
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;          // 14 warps
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
 
 constexpr int kLStage = kKeys * kMaxRC * 2;       // 32 KB
@@ -56,7 +57,8 @@ constexpr int kXBytes = kRows * kKeys * 4;        // 32 KB per receive buffer
 constexpr int kOffL = 0;
 constexpr int kOffP = kOffL + kStages * kLStage;
 constexpr int kOffX = kOffP + 2 * kPBytes;        // also the staging area of q' (64 KB)
-constexpr int kOffBar = kOffX + 2 * kXBytes;
+constexpr int kOffRed = kOffX + 2 * kXBytes;      // 2 x 128 floats: softmax warp-pair exchange
+constexpr int kOffBar = kOffRed + 1024;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;   // + barriers + alignment slack
 
 constexpr uint32_t kTmemO = 0;       // columns [0, RC)
@@ -99,6 +101,29 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int si
 // eight consecutive rows hit eight different bank groups.
 __device__ __forceinline__ uint32_t x_offset(uint32_t r, uint32_t c) {
   return r * 256u + (((c & 8u) | ((c ^ r) & 7u)) << 4);
+}
+
+// Pairwise (tree) max / sum of 32 values: log-depth dependency chains.
+__device__ __forceinline__ float tree_max32(const float (&v)[32]) {
+  float a[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) a[c] = fmaxf(v[c], v[c + 16]);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) a[c] = fmaxf(a[c], a[c + 8]);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) a[c] = fmaxf(a[c], a[c + 4]);
+  return fmaxf(fmaxf(a[0], a[2]), fmaxf(a[1], a[3]));
+}
+
+__device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
+  float a[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) a[c] = v[c] + v[c + 16];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) a[c] = a[c] + a[c + 8];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) a[c] = a[c] + a[c + 4];
+  return (a[0] + a[2]) + (a[1] + a[3]);
 }
 
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&s)[64]) {
@@ -147,18 +172,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_ready, 128);
+    mbar_init(&bars->q_ready, 256);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->l_full[s], 1);
       mbar_init(&bars->l_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], a.pair ? 256 : 128);
-      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->s_empty[i], a.pair ? 384 : 256);
+      mbar_init(&bars->p_full[i], 256);
       mbar_init(&bars->p_empty[i], 1);
-      mbar_init(&bars->x_full[i], 128);
-      mbar_init(&bars->x_empty[i], 128);
+      mbar_init(&bars->x_full[i], 1);      // armed by one local thread; bytes from the peer
+      mbar_init(&bars->x_empty[i], 8);     // one arrival per softmax warp of the peer
     }
     mbar_init(&bars->o_last, 1);
     bars->abort_flag = 0;
@@ -249,21 +274,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bi = j & 1, k = j >> 1;
         if (!warp_wait(&bars->s_full[bi], k & 1, 40, abort_flag)) break;
         tc_fence_after();
-        float v[64];
-        tmem_ld64(tmem + lane_base + kTmemS + bi * kKeys, v);
-        tc_fence_before();
-        mbar_arrive(&bars->s_empty[bi]);
         if (!warp_wait<true>(&bars->x_empty[bi], k & 1, 41, abort_flag)) break;
         const uint32_t dst = x_peer0 + bi * kXBytes;
+        const uint32_t bar = bi ? xfull_peer1 : xfull_peer0;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_cluster_v4(dst + x_offset(r, c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-        mbar_arrive_remote(bi ? xfull_peer1 : xfull_peer0);
+        for (int hh = 0; hh < 2; ++hh) {          // two 32-column halves
+          float v[32];
+          tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys + hh * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_async_v4(dst + x_offset(r, hh * 8 + c), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                        v[4 * c + 3], bar);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->s_empty[bi]);
       }
     }
   } else {
     // ======================= softmax / epilogue =======================
+    // Two warps per TMEM lane quadrant: the same 32 rows, keys split in halves
+    // of 32 (and O's columns split in halves for rescaling and the epilogue).
     const int qd = warp & 3;                      // TMEM lane quadrant
+    const int half = (warp - 6) >> 2;             // 0: keys 0..31, 1: keys 32..63
     const int r = qd * 32 + lane;                 // row within the tile
     const int grow = row0 + r;                    // row within batch entry b
     const bool row_valid = grow < rows_b;
@@ -272,110 +305,130 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t x_local = smem_u32(sX);
     const uint32_t xempty_peer0 = a.pair ? mapa_shared(smem_u32(&bars->x_empty[0]), peer) : 0u;
     const uint32_t xempty_peer1 = a.pair ? mapa_shared(smem_u32(&bars->x_empty[1]), peer) : 0u;
+    float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2][128] partner exchange
+    const uint32_t bar_id = 1u + (uint32_t)qd;               // named barrier of the warp pair
+    const int oc0 = half * (RC / 2);                          // O columns handled by this warp
 
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_half = 0.f;
     bool ok = nt > 0;
     if (ok) {
       // q' (staged by TMA in the receive buffers, 128-byte swizzled rows) -> TMEM
       ok = warp_wait(&bars->q_full, 0, 29, abort_flag);
       if (ok) {
         const uint32_t qs = x_local;
-        for (int kc = 0; kc < nchunk; ++kc) {
-          uint32_t u[32];
-#pragma unroll
+        for (int kc = half; kc < nchunk; kc += 2) {
+#pragma unroll 1
           for (int c = 0; c < 8; ++c) {
+            uint32_t u0, u1, u2, u3;
             const uint32_t addr = qs + kc * (kRows * 128) + sw128_offset((uint32_t)r, (uint32_t)c);
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(u[4 * c]), "=r"(u[4 * c + 1]), "=r"(u[4 * c + 2]),
-                           "=r"(u[4 * c + 3])
+                         : "=r"(u0), "=r"(u1), "=r"(u2), "=r"(u3)
                          : "r"(addr)
                          : "memory");
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             tmem + lane_base + kTmemQ + kc * 32 + c * 4),
+                         "r"(u0), "r"(u1), "r"(u2), "r"(u3)
+                         : "memory");
           }
-          tmem_st32u(tmem + lane_base + kTmemQ + kc * 32, u);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->q_ready);
         if (a.pair) {                 // my receive buffers may now be written by the peer
-          mbar_arrive_remote(xempty_peer0);
-          mbar_arrive_remote(xempty_peer1);
+          if (warp == 6 && lane == 0) {   // arm the receive barriers of tiles 0 and 1
+            mbar_arrive_expect_tx(&bars->x_full[0], (uint32_t)kXBytes);
+            if (nt > 1) mbar_arrive_expect_tx(&bars->x_full[1], (uint32_t)kXBytes);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            fence_acq_rel_cluster();
+            mbar_arrive_remote(xempty_peer0);
+            mbar_arrive_remote(xempty_peer1);
+          }
         }
       }
     }
     for (int j = 0; j < nt && ok; ++j) {
       const int bi = j & 1, k = j >> 1;
-      float s[kKeys];
+      float s[32];
       if (!warp_wait(&bars->s_full[bi], k & 1, 30, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      tmem_ld64(tmem + lane_base + kTmemS + bi * kKeys, s);
+      tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys + half * 32, s);
+      tmem_wait_ld();
 
       if (a.pair) {
-        // the peer's partial S over its half of the rank
+        // the peer's partial S over its half of the rank (my 32 keys)
         if (!warp_wait<true>(&bars->x_full[bi], k & 1, 32, abort_flag)) { ok = false; break; }
         const uint32_t src = x_local + bi * kXBytes;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < 8; ++c) {
           float x0, x1, x2, x3;
-          ld_shared_v4f(src + x_offset(r, c), x0, x1, x2, x3);
+          ld_shared_v4f(src + x_offset(r, half * 8 + c), x0, x1, x2, x3);
           s[4 * c] += x0;
           s[4 * c + 1] += x1;
           s[4 * c + 2] += x2;
           s[4 * c + 3] += x3;
         }
-        mbar_arrive_remote(bi ? xempty_peer1 : xempty_peer0);
+        // re-arm this buffer's barrier for tile j+2 (its phase for tile j is complete)
+        if (warp == 6 && lane == 0 && j + 2 < nt)
+          mbar_arrive_expect_tx(&bars->x_full[bi], (uint32_t)kXBytes);
+        __syncwarp();
+        if (lane == 0) {
+          fence_acq_rel_cluster();
+          mbar_arrive_remote(bi ? xempty_peer1 : xempty_peer0);
+        }
       }
       tc_fence_before();
       mbar_arrive(&bars->s_empty[bi]);
 
       // mask: key s_idx visible iff s_idx < Tkv and (not causal or s_idx <= t)
-      const int key0 = (tile0 + j) * kKeys;
+      const int key0 = (tile0 + j) * kKeys + half * 32;
       const int lim = a.causal ? min(t_row + 1, a.Tkv) : a.Tkv;   // visible keys < lim
-      float mx = -INFINITY;
-      if (!row_valid || key0 + kKeys > lim) {
+      if (!row_valid || key0 + 32 > lim) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c)
+        for (int c = 0; c < 32; ++c)
           if (!row_valid || key0 + c >= lim) s[c] = -INFINITY;
       }
-#pragma unroll
-      for (int c = 0; c < kKeys; ++c) mx = fmaxf(mx, s[c]);
+      const float mx_half = tree_max32(s);
+      // row max over both halves through shared memory
+      red[half * 128 + r] = mx_half;
+      named_bar_sync(bar_id, 64);
+      const float mx = fmaxf(mx_half, red[(half ^ 1) * 128 + r]);
+      named_bar_sync(bar_id, 64);
       const float m_new = fmaxf(m_run, mx);
       const bool grow_max = m_new > m_run + kRescaleThreshold;   // false while both -inf
       const float m_ref = grow_max ? m_new : m_run;
       const float alpha = grow_max ? ex2(m_run - m_new) : 1.f;   // m_run = -inf -> 0
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float psum = 0.f;
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        s[c] = ex2(s[c] - m_use);
-        psum += s[c];
-      }
-      l_run = l_run * alpha + psum;
+      for (int c = 0; c < 32; ++c) s[c] = ex2(s[c] - m_use);
+      l_half = l_half * alpha + tree_sum32(s);
       m_run = m_ref;
 
-      // rescale O_lat (only after the previous P.L has landed)
+      // rescale my half of O_lat's columns (only after the previous P.L has landed)
       if (__any_sync(0xffffffffu, grow_max && j > 0)) {
         if (!warp_wait(&bars->p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, 33, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int c = 0; c < RC; c += 32) {
-          float o[32];
-          tmem_ld32(tmem + lane_base + kTmemO + c, o);
+        for (int c = oc0; c < oc0 + RC / 2; c += 16) {
+          float o[16];
+          tmem_ld16(tmem + lane_base + kTmemO + c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tmem + lane_base + kTmemO + c, o);
+          for (int e = 0; e < 16; ++e) o[e] *= alpha;
+          tmem_st16(tmem + lane_base + kTmemO + c, o);
         }
         tmem_wait_st();
       }
 
-      // P (bf16) into the K-major swizzled P buffer
+      // P (bf16) into the K-major swizzled P buffer: my 4 of the row's 8 chunks
       if (!warp_wait(&bars->p_empty[bi], (k & 1) ^ 1, 34, abort_flag)) { ok = false; break; }
       const uint32_t pb = smem_u32(sP + bi * kPBytes);
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared_v4(pb + sw128_offset(r, c), pack_bf16x2(s[8 * c], s[8 * c + 1]),
+      for (int c = 0; c < 4; ++c)
+        st_shared_v4(pb + sw128_offset(r, half * 4 + c), pack_bf16x2(s[8 * c], s[8 * c + 1]),
                      pack_bf16x2(s[8 * c + 2], s[8 * c + 3]),
                      pack_bf16x2(s[8 * c + 4], s[8 * c + 5]),
                      pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
@@ -385,6 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- epilogue ----------------
+    // the row sum is the two halves' sums (added in the same order in both warps)
+    red[half * 128 + r] = l_half;
+    named_bar_sync(bar_id, 64);
+    const float l_run = red[r] + red[128 + r];
     const int64_t gr = (int64_t)b * rows_b + grow;     // row in (B*Tq*H)
     const int64_t nrows = (int64_t)a.B * rows_b;
     bool have_o = false;
@@ -395,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (a.splits == 1) {
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.olat) + gr * a.R + c0;
-      for (int c = 0; c < RC; c += 32) {
+      for (int c = oc0; c < oc0 + RC / 2; c += 32) {
         float o[32];
         if (have_o) {
           tmem_ld32(tmem + lane_base + kTmemO + c, o);
@@ -416,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       float* dst = a.part_o + ((int64_t)sp * nrows + gr) * a.R + c0;
-      for (int c = 0; c < RC; c += 32) {
+      for (int c = oc0; c < oc0 + RC / 2; c += 32) {
         float o[32];
         if (have_o) {
           tmem_ld32(tmem + lane_base + kTmemO + c, o);
@@ -432,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             d4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
         }
       }
-      if (row_valid && crank == 0) {
+      if (row_valid && crank == 0 && half == 0) {
         float* ml = a.part_ml + ((int64_t)sp * nrows + gr) * 2;
         ml[0] = have_o ? m_run : -INFINITY;
         ml[1] = have_o ? l_run : 0.f;
