@@ -46,17 +46,17 @@ namespace {
 
 constexpr int kRows = 128;           // rows per CTA tile (MMA M)
 constexpr int kKeys = 64;            // keys per tile (S MMA N, O MMA K)
-constexpr int kStages = 4;           // latent tile ring
+constexpr int kStages = 5;           // latent tile ring
 constexpr int kMaxRC = 256;          // rank columns per CTA
 constexpr int kThreads = 448;          // 14 warps
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
 
 constexpr int kLStage = kKeys * kMaxRC * 2;       // 32 KB
 constexpr int kPBytes = kRows * kKeys * 2;        // 16 KB
-constexpr int kXBytes = kRows * kKeys * 4;        // 32 KB per receive buffer
+constexpr int kXBytes = kRows * kKeys * 2;        // 16 KB per receive buffer (fp16 partial S)
 constexpr int kOffL = 0;
-constexpr int kOffP = kOffL + kStages * kLStage;
-constexpr int kOffX = kOffP + 2 * kPBytes;        // also the staging area of q' (64 KB)
+constexpr int kOffP = kOffL + kStages * kLStage;  // P and receive buffers: staging of q' (64 KB)
+constexpr int kOffX = kOffP + 2 * kPBytes;
 constexpr int kOffRed = kOffX + 2 * kXBytes;      // 2 x 128 floats: softmax warp-pair exchange
 constexpr int kOffBar = kOffRed + 1024;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;   // + barriers + alignment slack
@@ -96,13 +96,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int si
   return __all_sync(0xffffffffu, ok);
 }
 
-// Position of 16-byte chunk c (0..15) of row r in the 256-byte rows of a
-// receive buffer; the low three chunk bits are XOR-ed with the row so that
-// eight consecutive rows hit eight different bank groups.
-__device__ __forceinline__ uint32_t x_offset(uint32_t r, uint32_t c) {
-  return r * 256u + (((c & 8u) | ((c ^ r) & 7u)) << 4);
-}
-
 // Pairwise (tree) max / sum of 32 values: log-depth dependency chains.
 __device__ __forceinline__ float tree_max32(const float (&v)[32]) {
   float a[16];
@@ -124,14 +117,6 @@ __device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) a[c] = a[c] + a[c + 4];
   return (a[0] + a[2]) + (a[1] + a[3]);
-}
-
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&s)[64]) {
-  float(&a0)[32] = *reinterpret_cast<float(*)[32]>(&s[0]);
-  float(&a1)[32] = *reinterpret_cast<float(*)[32]>(&s[32]);
-  tmem_ld32(taddr, a0);
-  tmem_ld32(taddr + 32, a1);
-  tmem_wait_ld();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -203,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&mapL);
       mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
       for (int kc = 0; kc < nchunk; ++kc)
-        tma_load_3d(sX + kc * (kRows * 128), &mapQ, &bars->q_full, c0 + 64 * kc, row0, b);
+        tma_load_3d(sP + kc * (kRows * 128), &mapQ, &bars->q_full, c0 + 64 * kc, row0, b);
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int st = j % kStages;
@@ -243,22 +228,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bars->l_empty[jj % kStages]);
         return true;
       };
-      for (int j = 0; j < nt && ok; ++j) {
-        const int st = j % kStages;
-        if (!mbar_wait(&bars->l_full[st], (j / kStages) & 1, 22, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(&bars->s_empty[j & 1], ((j >> 1) & 1) ^ 1, 23, abort_flag)) { ok = false; break; }
+      // S(jj) = q' L(jj)^T into S buffer jj&1, once the consumers of S(jj-2) let go
+      auto issue_s = [&](int jj) -> bool {
+        const int st = jj % kStages;
+        if (!mbar_wait(&bars->l_full[st], (jj / kStages) & 1, 22, abort_flag)) return false;
+        if (!mbar_wait(&bars->s_empty[jj & 1], ((jj >> 1) & 1) ^ 1, 23, abort_flag)) return false;
         tc_fence_after();
         const uint32_t lst = l0 + st * kLStage;
-        const uint32_t sbuf = tmem + kTmemS + (j & 1) * kKeys;
-        for (int k = 0; k < RC / 16; ++k) {
-          const uint64_t bd = make_sdesc_sw128(lst + (k >> 2) * (kKeys * 128) + (k & 3) * 32, 16,
-                                               1024);
-          umma_bf16_ta(sbuf, tmem + kTmemQ + k * 8, bd, idesc_s, k > 0 ? 1u : 0u);
+        const uint32_t sbuf = tmem + kTmemS + (jj & 1) * kKeys;
+        const uint64_t bd0 = make_sdesc_sw128(lst, 16, 1024);
+        for (int kc = 0; kc < RC / 64; ++kc) {
+#pragma unroll
+          for (int kw = 0; kw < 4; ++kw)
+            umma_bf16_ta(sbuf, tmem + kTmemQ + (kc * 4 + kw) * 8,
+                         bd0 + (uint64_t)((kc * (kKeys * 128) + kw * 32) >> 4), idesc_s,
+                         (kc | kw) != 0 ? 1u : 0u);
         }
-        umma_commit(&bars->s_full[j & 1]);
-        if (j > 0 && !issue_o(j - 1)) { ok = false; break; }
+        umma_commit(&bars->s_full[jj & 1]);
+        return true;
+      };
+      // Order: S(0), S(1), then per tile j: S(j+2) as soon as S(j) has been read
+      // (it overlaps the softmax of tile j), then O(j) once P(j) is written.
+      if (ok) ok = issue_s(0);
+      if (ok && nt > 1) ok = issue_s(1);
+      for (int j = 0; j < nt && ok; ++j) {
+        if (j + 2 < nt && !issue_s(j + 2)) { ok = false; break; }
+        if (!issue_o(j)) { ok = false; break; }
       }
-      if (ok) issue_o(nt - 1);
       umma_commit(&bars->o_last);
     }
   } else if (warp < 6) {
@@ -278,14 +274,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = x_peer0 + bi * kXBytes;
         const uint32_t bar = bi ? xfull_peer1 : xfull_peer0;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {          // two 32-column halves
+        for (int hh = 0; hh < 2; ++hh) {          // two 32-column halves, sent as fp16
           float v[32];
           tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys + hh * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_async_v4(dst + x_offset(r, hh * 8 + c), v[4 * c], v[4 * c + 1], v[4 * c + 2],
-                        v[4 * c + 3], bar);
+          for (int c = 0; c < 4; ++c)
+            st_async_v4u(dst + sw128_offset(r, hh * 4 + c), pack_half2(v[8 * c], v[8 * c + 1]),
+                         pack_half2(v[8 * c + 2], v[8 * c + 3]),
+                         pack_half2(v[8 * c + 4], v[8 * c + 5]),
+                         pack_half2(v[8 * c + 6], v[8 * c + 7]), bar);
         }
         tc_fence_before();
         mbar_arrive(&bars->s_empty[bi]);
@@ -315,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // q' (staged by TMA in the receive buffers, 128-byte swizzled rows) -> TMEM
       ok = warp_wait(&bars->q_full, 0, 29, abort_flag);
       if (ok) {
-        const uint32_t qs = x_local;
+        const uint32_t qs = smem_u32(sP);
         for (int kc = half; kc < nchunk; kc += 2) {
 #pragma unroll 1
           for (int c = 0; c < 8; ++c) {
@@ -361,13 +359,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait<true>(&bars->x_full[bi], k & 1, 32, abort_flag)) { ok = false; break; }
         const uint32_t src = x_local + bi * kXBytes;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float x0, x1, x2, x3;
-          ld_shared_v4f(src + x_offset(r, half * 8 + c), x0, x1, x2, x3);
-          s[4 * c] += x0;
-          s[4 * c + 1] += x1;
-          s[4 * c + 2] += x2;
-          s[4 * c + 3] += x3;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u0, u1, u2, u3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(u0), "=r"(u1), "=r"(u2), "=r"(u3)
+                       : "r"(src + sw128_offset((uint32_t)r, (uint32_t)(half * 4 + c)))
+                       : "memory");
+          const float2 f0 = unpack_half2(u0), f1 = unpack_half2(u1);
+          const float2 f2 = unpack_half2(u2), f3 = unpack_half2(u3);
+          s[8 * c] += f0.x; s[8 * c + 1] += f0.y;
+          s[8 * c + 2] += f1.x; s[8 * c + 3] += f1.y;
+          s[8 * c + 4] += f2.x; s[8 * c + 5] += f2.y;
+          s[8 * c + 6] += f3.x; s[8 * c + 7] += f3.y;
         }
         // re-arm this buffer's barrier for tile j+2 (its phase for tile j is complete)
         if (warp == 6 && lane == 0 && j + 2 < nt)

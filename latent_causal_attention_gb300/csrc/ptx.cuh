@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace mla {
@@ -368,6 +369,24 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
       "[%5];" ::"r"(addr),
       "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
       : "memory");
+}
+
+__device__ __forceinline__ void st_async_v4u(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_half2(uint32_t u) {
+  return __half22float2(*reinterpret_cast<__half2*>(&u));
 }
 
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c,
