@@ -119,6 +119,7 @@ __device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
   return (a[0] + a[2]) + (a[1] + a[3]);
 }
 
+template <int kRC>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_packed_kernel(const __grid_constant__ CUtensorMap mapQ,
                         const __grid_constant__ CUtensorMap mapL, FlashArgs a) {
@@ -151,9 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int per_split = (n_tiles_all + a.splits - 1) / a.splits;
   const int tile0 = sp * per_split;
   const int nt = max(0, min(n_tiles_all, tile0 + per_split) - tile0);
-  const int RC = a.RC;
+  constexpr int RC = kRC;                  // rank columns per CTA
   const int c0 = (int)crank * RC;          // first rank column of this CTA
-  const int nchunk = RC / 64;
+  constexpr int nchunk = RC / 64;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -207,53 +208,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
+    // Descriptors are built once per tile and advanced by constants; the issue
+    // sequence is fully unrolled (a single thread issuing tcgen05.mma is the
+    // rate limit for the narrow S MMAs otherwise).  Per tile j, the four long
+    // O(j) += P(j) L(j) MMAs (N = RC) are interleaved with the narrow
+    // S(j+2) = q' L(j+2)^T MMAs (N = 64), so the tensor core always has queued
+    // work while the next instruction is issued.
     if (lane == 0 && nt > 0) {
-      const uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
-      const uint32_t idesc_o = make_idesc_bf16(kRows, RC, false, true);
+      constexpr uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
+      constexpr uint32_t idesc_o = make_idesc_bf16(kRows, kRC, false, true);
+      constexpr int kSSteps = kRC / 16;            // K-steps of one S tile
+      constexpr int kSPerO = kSSteps / 4;          // S K-steps per O K-step
       const uint32_t l0 = smem_u32(sL), p0 = smem_u32(sP);
+      const uint32_t tq = tmem + kTmemQ;
       bool ok = mbar_wait(&bars->q_ready, 0, 20, abort_flag);
       tc_fence_after();
-      auto issue_o = [&](int jj) -> bool {
-        if (!mbar_wait(&bars->p_full[jj & 1], (jj >> 1) & 1, 21, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t lst = l0 + (jj % kStages) * kLStage;
-        const uint32_t pb = p0 + (jj & 1) * kPBytes;
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t ad = make_sdesc_sw128(pb + kk * 32, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(lst + kk * 2048, kKeys * 128, 1024);
-          umma_bf16(tmem + kTmemO, ad, bd, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&bars->p_empty[jj & 1]);
-        umma_commit(&bars->l_empty[jj % kStages]);
-        return true;
-      };
-      // S(jj) = q' L(jj)^T into S buffer jj&1, once the consumers of S(jj-2) let go
-      auto issue_s = [&](int jj) -> bool {
+      // wait for latent tile jj and the release of S buffer jj&1; returns the B descriptor
+      auto prep_s = [&](int jj, uint64_t& bd) -> bool {
         const int st = jj % kStages;
         if (!mbar_wait(&bars->l_full[st], (jj / kStages) & 1, 22, abort_flag)) return false;
         if (!mbar_wait(&bars->s_empty[jj & 1], ((jj >> 1) & 1) ^ 1, 23, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t lst = l0 + st * kLStage;
-        const uint32_t sbuf = tmem + kTmemS + (jj & 1) * kKeys;
-        const uint64_t bd0 = make_sdesc_sw128(lst, 16, 1024);
-        for (int kc = 0; kc < RC / 64; ++kc) {
-#pragma unroll
-          for (int kw = 0; kw < 4; ++kw)
-            umma_bf16_ta(sbuf, tmem + kTmemQ + (kc * 4 + kw) * 8,
-                         bd0 + (uint64_t)((kc * (kKeys * 128) + kw * 32) >> 4), idesc_s,
-                         (kc | kw) != 0 ? 1u : 0u);
-        }
-        umma_commit(&bars->s_full[jj & 1]);
+        bd = make_sdesc_sw128(l0 + st * kLStage, 16, 1024);
         return true;
       };
-      // Order: S(0), S(1), then per tile j: S(j+2) as soon as S(j) has been read
-      // (it overlaps the softmax of tile j), then O(j) once P(j) is written.
-      if (ok) ok = issue_s(0);
-      if (ok && nt > 1) ok = issue_s(1);
+      // S K-step k of a tile: A = q' columns [8k, 8k+8) of TMEM, B = latent K-chunk k/4
+#define MLA_S_STEP(sbuf, bd, k)                                                          \
+  umma_bf16_ta((sbuf), tq + (k) * 8,                                                     \
+               (bd) + (uint64_t)((((k) >> 2) * (kKeys * 128) + ((k) & 3) * 32) >> 4), idesc_s, \
+               (k) > 0 ? 1u : 0u)
+      for (int jj = 0; jj < 2 && jj < nt && ok; ++jj) {
+        uint64_t bd;
+        if (!prep_s(jj, bd)) { ok = false; break; }
+        const uint32_t sbuf = tmem + kTmemS + jj * kKeys;
+#pragma unroll
+        for (int k = 0; k < kSSteps; ++k) MLA_S_STEP(sbuf, bd, k);
+        umma_commit(&bars->s_full[jj]);
+      }
       for (int j = 0; j < nt && ok; ++j) {
-        if (j + 2 < nt && !issue_s(j + 2)) { ok = false; break; }
-        if (!issue_o(j)) { ok = false; break; }
+        const bool has_s = j + 2 < nt;
+        uint64_t bds = 0;
+        if (has_s && !prep_s(j + 2, bds)) { ok = false; break; }
+        if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, 21, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t ad = make_sdesc_sw128(p0 + (j & 1) * kPBytes, 16, 1024);
+        const uint64_t bdo = make_sdesc_sw128(l0 + (j % kStages) * kLStage, kKeys * 128, 1024);
+        const uint32_t sbuf = tmem + kTmemS + (j & 1) * kKeys;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          umma_bf16(tmem + kTmemO, ad + (uint64_t)((kk * 32) >> 4),
+                    bdo + (uint64_t)((kk * 2048) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          if (has_s) {
+#pragma unroll
+            for (int q = 0; q < kSPerO; ++q) MLA_S_STEP(sbuf, bds, kk * kSPerO + q);
+          }
+        }
+#undef MLA_S_STEP
+        umma_commit(&bars->p_empty[j & 1]);
+        umma_commit(&bars->l_empty[j % kStages]);
+        if (has_s) umma_commit(&bars->s_full[j & 1]);
       }
       umma_commit(&bars->o_last);
     }
@@ -337,9 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&bars->x_full[0], (uint32_t)kXBytes);
             if (nt > 1) mbar_arrive_expect_tx(&bars->x_full[1], (uint32_t)kXBytes);
           }
+          // every lane's reads are consumed before __syncwarp, which orders them
+          // before lane 0's release-arrive; the peer acquires before writing
           __syncwarp();
           if (lane == 0) {
-            fence_acq_rel_cluster();
             mbar_arrive_remote(xempty_peer0);
             mbar_arrive_remote(xempty_peer1);
           }
@@ -376,10 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 6 && lane == 0 && j + 2 < nt)
           mbar_arrive_expect_tx(&bars->x_full[bi], (uint32_t)kXBytes);
         __syncwarp();
-        if (lane == 0) {
-          fence_acq_rel_cluster();
-          mbar_arrive_remote(bi ? xempty_peer1 : xempty_peer0);
-        }
+        if (lane == 0) mbar_arrive_remote(bi ? xempty_peer1 : xempty_peer0);
       }
       tc_fence_before();
       mbar_arrive(&bars->s_empty[bi]);
@@ -553,9 +564,10 @@ __global__ void merge_partials_kernel(const float* __restrict__ ml, int ml_strid
 
 }  // namespace
 
-cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL,
-                                const FlashArgs& args, cudaStream_t stream) {
-  auto kern = flash_packed_kernel;
+template <int kRC>
+static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                  const FlashArgs& args, cudaStream_t stream) {
+  auto kern = flash_packed_kernel<kRC>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -576,6 +588,17 @@ cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL
   e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                const FlashArgs& args, cudaStream_t stream) {
+  switch (args.RC) {
+    case 64: return launch_flash_rc<64>(mapQ, mapL, args, stream);
+    case 128: return launch_flash_rc<128>(mapQ, mapL, args, stream);
+    case 192: return launch_flash_rc<192>(mapQ, mapL, args, stream);
+    case 256: return launch_flash_rc<256>(mapQ, mapL, args, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t flash_read_device_error(unsigned int* code, int clear) {
