@@ -223,51 +223,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tq = tmem + kTmemQ;
       bool ok = mbar_wait(&bars->q_ready, 0, 20, abort_flag);
       tc_fence_after();
-      // wait for latent tile jj and the release of S buffer jj&1; returns the B descriptor
-      auto prep_s = [&](int jj, uint64_t& bd) -> bool {
-        const int st = jj % kStages;
-        if (!mbar_wait(&bars->l_full[st], (jj / kStages) & 1, 22, abort_flag)) return false;
-        if (!mbar_wait(&bars->s_empty[jj & 1], ((jj >> 1) & 1) ^ 1, 23, abort_flag)) return false;
-        tc_fence_after();
-        bd = make_sdesc_sw128(l0 + st * kLStage, 16, 1024);
-        return true;
-      };
       // S K-step k of a tile: A = q' columns [8k, 8k+8) of TMEM, B = latent K-chunk k/4
 #define MLA_S_STEP(sbuf, bd, k)                                                          \
   umma_bf16_ta((sbuf), tq + (k) * 8,                                                     \
                (bd) + (uint64_t)((((k) >> 2) * (kKeys * 128) + ((k) & 3) * 32) >> 4), idesc_s, \
                (k) > 0 ? 1u : 0u)
-      for (int jj = 0; jj < 2 && jj < nt && ok; ++jj) {
-        uint64_t bd;
-        if (!prep_s(jj, bd)) { ok = false; break; }
-        const uint32_t sbuf = tmem + kTmemS + jj * kKeys;
-#pragma unroll
-        for (int k = 0; k < kSSteps; ++k) MLA_S_STEP(sbuf, bd, k);
-        umma_commit(&bars->s_full[jj]);
-      }
-      for (int j = 0; j < nt && ok; ++j) {
-        const bool has_s = j + 2 < nt;
-        uint64_t bds = 0;
-        if (has_s && !prep_s(j + 2, bds)) { ok = false; break; }
-        if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, 21, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t ad = make_sdesc_sw128(p0 + (j & 1) * kPBytes, 16, 1024);
-        const uint64_t bdo = make_sdesc_sw128(l0 + (j % kStages) * kLStage, kKeys * 128, 1024);
-        const uint32_t sbuf = tmem + kTmemS + (j & 1) * kKeys;
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          umma_bf16(tmem + kTmemO, ad + (uint64_t)((kk * 32) >> 4),
-                    bdo + (uint64_t)((kk * 2048) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-          if (has_s) {
-#pragma unroll
-            for (int q = 0; q < kSPerO; ++q) MLA_S_STEP(sbuf, bds, kk * kSPerO + q);
+      // Small scheduler: S(js) as soon as latent tile js has landed and the
+      // readers of S(js-2) have let its buffer go; O(jo) as soon as P(jo) is
+      // written.  When both are ready, the narrow S K-steps are interleaved
+      // with the long O K-steps so the tensor core always has queued work.
+      int js = 0, jo = 0;
+      const unsigned long long t_start = globaltimer_ns();
+      unsigned spins = 0;
+      while (ok && jo < nt) {
+        const bool s_ready =
+            js < nt && mbar_test(smem_u32(&bars->l_full[js % kStages]), (js / kStages) & 1) &&
+            mbar_test(smem_u32(&bars->s_empty[js & 1]), ((js >> 1) & 1) ^ 1);
+        const bool o_ready = jo < js && mbar_test(smem_u32(&bars->p_full[jo & 1]), (jo >> 1) & 1);
+        if (!s_ready && !o_ready) {
+          if ((++spins & 1023u) == 0 &&
+              (*abort_flag || globaltimer_ns() - t_start > kWaitLimitNs * 8)) {
+            report_error(kErrWaitTimeout | 21u);
+            *abort_flag = 1;
+            ok = false;
           }
+          continue;
         }
-#undef MLA_S_STEP
-        umma_commit(&bars->p_empty[j & 1]);
-        umma_commit(&bars->l_empty[j % kStages]);
-        if (has_s) umma_commit(&bars->s_full[j & 1]);
+        tc_fence_after();
+        uint64_t bds = 0;
+        uint32_t sbuf = 0;
+        if (s_ready) {
+          bds = make_sdesc_sw128(l0 + (js % kStages) * kLStage, 16, 1024);
+          sbuf = tmem + kTmemS + (js & 1) * kKeys;
+        }
+        if (o_ready) {
+          const uint64_t ad = make_sdesc_sw128(p0 + (jo & 1) * kPBytes, 16, 1024);
+          const uint64_t bdo = make_sdesc_sw128(l0 + (jo % kStages) * kLStage, kKeys * 128, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            umma_bf16(tmem + kTmemO, ad + (uint64_t)((kk * 32) >> 4),
+                      bdo + (uint64_t)((kk * 2048) >> 4), idesc_o, (jo > 0 || kk > 0) ? 1u : 0u);
+            if (s_ready) {
+#pragma unroll
+              for (int q = 0; q < kSPerO; ++q) MLA_S_STEP(sbuf, bds, kk * kSPerO + q);
+            }
+          }
+          umma_commit(&bars->p_empty[jo & 1]);
+          umma_commit(&bars->l_empty[jo % kStages]);
+          ++jo;
+        } else {
+#pragma unroll
+          for (int k = 0; k < kSSteps; ++k) MLA_S_STEP(sbuf, bds, k);
+        }
+        if (s_ready) {
+          umma_commit(&bars->s_full[js & 1]);
+          ++js;
+        }
       }
+#undef MLA_S_STEP
       umma_commit(&bars->o_last);
     }
   } else if (warp < 6) {
@@ -367,6 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys + half * 32, s);
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars->s_empty[bi]);      // S(j) is in registers: the buffer may be refilled
 
       if (a.pair) {
         // the peer's partial S over its half of the rank (my 32 keys)
@@ -392,8 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(bi ? xempty_peer1 : xempty_peer0);
       }
-      tc_fence_before();
-      mbar_arrive(&bars->s_empty[bi]);
 
       // mask: key s_idx visible iff s_idx < Tkv and (not causal or s_idx <= t)
       const int key0 = (tile0 + j) * kKeys + half * 32;
