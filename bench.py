@@ -102,6 +102,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def flash_traffic():
+    """DRAM bytes per launch of the prefill flash kernel from the committed ncu
+    capture, or None when the kernel source changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "flash_prefill_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for name in ("flash_tc.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "latent_causal_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != rec.get("source_sha256_16"):
+        return None
+    return int(rec["traffic_bytes_per_launch"])
+
+
 # ------------------------------------------------------------------ oracle timing
 _ORACLE_CACHE = {}
 
@@ -332,7 +351,8 @@ def run_ours(args, rank: int, world: int):
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} bf16 dense (burst)",
-                     "flops_per_launch": flops_flash, "traffic": None},
+                     "flops_per_launch": flops_flash, "traffic": flash_traffic(),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": int(launches),
