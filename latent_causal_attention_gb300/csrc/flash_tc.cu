@@ -29,11 +29,12 @@
 // the identical softmax (a + b is the same bits in either CTA) and accumulate
 // their half of O_lat.
 //
-// Warp roles (448 threads): warp 0 lane 0 = TMA producer (q' once, then a
+// Warp roles (480 threads): warp 0 lane 0 = TMA producer (q' once, then a
 // 4-stage ring of latent tiles); warp 1 = TMEM owner, lane 0 issues MMAs;
 // warps 2-5 = partial-S exchange (CTA pair only); warps 6-13 = softmax and
 // epilogue, two warps per row quadrant (each takes 32 of a tile's 64 keys and
-// half of O_lat's columns).  Warp w reads TMEM lanes 32*(w%4)..+31.
+// half of O_lat's columns); warp 14 forwards receive-buffer releases to the
+// peer (CTA pair only).  Warp w reads TMEM lanes 32*(w%4)..+31.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -48,7 +49,7 @@ constexpr int kRows = 128;           // rows per CTA tile (MMA M)
 constexpr int kKeys = 64;            // keys per tile (S MMA N, O MMA K)
 constexpr int kStages = 5;           // latent tile ring
 constexpr int kMaxRC = 256;          // rank columns per CTA
-constexpr int kThreads = 448;          // 14 warps
+constexpr int kThreads = 480;          // 15 warps
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
 
 constexpr int kLStage = kKeys * kMaxRC * 2;       // 32 KB
@@ -77,6 +78,7 @@ struct Bars {
   uint64_t o_last;
   uint64_t x_full[2];          // my receive buffer b was filled by the peer
   uint64_t x_empty[2];         // the peer's receive buffer b may be written again
+  uint64_t x_consumed[2];      // my softmax warps are done with my receive buffer b
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -169,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[i], 256);
       mbar_init(&bars->p_empty[i], 1);
       mbar_init(&bars->x_full[i], 1);      // armed by one local thread; bytes from the peer
-      mbar_init(&bars->x_empty[i], 8);     // one arrival per softmax warp of the peer
+      mbar_init(&bars->x_empty[i], 1);     // forwarded by the peer's forwarding warp
+      mbar_init(&bars->x_consumed[i], 8);  // one arrival per local softmax warp
     }
     mbar_init(&bars->o_last, 1);
     bars->abort_flag = 0;
@@ -241,7 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_test(smem_u32(&bars->s_empty[js & 1]), ((js >> 1) & 1) ^ 1);
         const bool o_ready = jo < js && mbar_test(smem_u32(&bars->p_full[jo & 1]), (jo >> 1) & 1);
         if (!s_ready && !o_ready) {
-          if ((++spins & 1023u) == 0 &&
+          // back off: this warp shares an SM sub-partition with softmax warps
+          __nanosleep(32);
+          if ((++spins & 255u) == 0 &&
               (*abort_flag || globaltimer_ns() - t_start > kWaitLimitNs * 8)) {
             report_error(kErrWaitTimeout | 21u);
             *abort_flag = 1;
@@ -315,6 +320,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->s_empty[bi]);
       }
     }
+  } else if (warp == 14) {
+    // ======================= release forwarding (CTA pair) =======================
+    // Passes "my receive buffer b is free" from the local softmax warps to the
+    // peer's x_empty[b]: the initial release of both buffers, then one per tile.
+    // The cluster-scope arrival is a round trip; keeping it on this warp keeps
+    // it off the softmax warps' path.
+    if (a.pair && nt > 0 && lane == 0) {
+      const uint32_t xe_peer0 = mapa_shared(smem_u32(&bars->x_empty[0]), peer);
+      const uint32_t xe_peer1 = mapa_shared(smem_u32(&bars->x_empty[1]), peer);
+      for (int n = 0; n < nt + 2; ++n) {
+        const int bi = n < 2 ? n : (n - 2) & 1;
+        const int ph = n < 2 ? 0 : ((n - 2) >> 1) + 1;     // completion index of x_consumed[bi]
+        if (!mbar_wait(&bars->x_consumed[bi], ph & 1, 45, abort_flag)) break;
+        mbar_arrive_remote(bi ? xe_peer1 : xe_peer0);
+      }
+    }
   } else {
     // ======================= softmax / epilogue =======================
     // Two warps per TMEM lane quadrant: the same 32 rows, keys split in halves
@@ -327,8 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_row = a.Tkv - a.Tq + (row_valid ? grow / a.H : 0);
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const uint32_t x_local = smem_u32(sX);
-    const uint32_t xempty_peer0 = a.pair ? mapa_shared(smem_u32(&bars->x_empty[0]), peer) : 0u;
-    const uint32_t xempty_peer1 = a.pair ? mapa_shared(smem_u32(&bars->x_empty[1]), peer) : 0u;
     float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2][128] partner exchange
     const uint32_t bar_id = 1u + (uint32_t)qd;               // named barrier of the warp pair
     const int oc0 = half * (RC / 2);                          // O columns handled by this warp
@@ -363,12 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&bars->x_full[0], (uint32_t)kXBytes);
             if (nt > 1) mbar_arrive_expect_tx(&bars->x_full[1], (uint32_t)kXBytes);
           }
-          // every lane's reads are consumed before __syncwarp, which orders them
-          // before lane 0's release-arrive; the peer acquires before writing
+          // every lane's reads are consumed before __syncwarp; the forwarding
+          // warp passes the release on to the peer
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive_remote(xempty_peer0);
-            mbar_arrive_remote(xempty_peer1);
+            mbar_arrive(&bars->x_consumed[0]);
+            mbar_arrive(&bars->x_consumed[1]);
           }
         }
       }
@@ -405,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 6 && lane == 0 && j + 2 < nt)
           mbar_arrive_expect_tx(&bars->x_full[bi], (uint32_t)kXBytes);
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(bi ? xempty_peer1 : xempty_peer0);
+        if (lane == 0) mbar_arrive(&bars->x_consumed[bi]);
       }
 
       // mask: key s_idx visible iff s_idx < Tkv and (not causal or s_idx <= t)
