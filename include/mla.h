@@ -117,6 +117,10 @@ size_t mla_latent_attention_workspace_size(int B, int Tq, int Tkv, int H, int d,
  *   - bf16 with d % 64 == 0, rank % 64 == 0, rank <= 512, d <= 256 and
  *     16-byte aligned pointers: tensor-core path (query absorbed into the
  *     latent space, flash loop over TMA-staged latent tiles with tcgen05).
+ *     With Tq >= 64 and d <= 128 it is one fused kernel per (head, 128
+ *     query positions) that also does the absorption and w_up_v and needs no
+ *     workspace; otherwise absorption GEMM, head-packed flash loop (split
+ *     over the key range when there are few rows), merge and w_up_v GEMM.
  *   - otherwise (fp32, or small/odd shapes): warp-per-query CUDA-core path
  *     (rank <= 1024, d <= 256).
  * Errors: MLA_ERR_NULL, MLA_ERR_SHAPE, MLA_ERR_DTYPE, MLA_ERR_ALIGN,

@@ -62,6 +62,12 @@ constexpr int kOffRed = kOffX + 2 * kXBytes;      // 2 x 128 floats: softmax war
 constexpr int kOffBar = kOffRed + 1024;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;   // + barriers + alignment slack
 
+// fused prefill staging inside the latent ring (before / after the loop):
+//   prologue: q tile at 0 (d/64 x 16 KB), w_up_k rows at 32 KB (d/64 x RC*128 B)
+//   epilogue: O_lat bf16 at 0 (RC/64 x 16 KB), w_up_v rows at 64 KB (d/64 x RC*128 B)
+constexpr int kFusedWkOff = 32 * 1024;
+constexpr int kFusedWvOff = 64 * 1024;
+
 constexpr uint32_t kTmemO = 0;       // columns [0, RC)
 constexpr uint32_t kTmemS = 256;     // two 64-column S buffers at 256, 320
 constexpr uint32_t kTmemQ = 384;     // q' as bf16 pairs, RC/2 columns
@@ -79,6 +85,12 @@ struct Bars {
   uint64_t x_full[2];          // my receive buffer b was filled by the peer
   uint64_t x_empty[2];         // the peer's receive buffer b may be written again
   uint64_t x_consumed[2];      // my softmax warps are done with my receive buffer b
+  uint64_t pro_full;           // fused prefill: q tile and w_up_k staged (TMA)
+  uint64_t pro_done;           // fused prefill: q . w_up_k^T computed into TMEM
+  uint64_t epi_a;              // fused prefill: normalised O_lat (bf16) written to smem
+  uint64_t epi_w;              // fused prefill: w_up_v staged (TMA)
+  uint64_t epi_done;           // fused prefill: O_lat . w_up_v computed into TMEM
+  uint64_t epi_x;              // fused prefill, CTA pair: the peer's partial output arrived
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -96,6 +108,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int si
                                           volatile int* abort) {
   const bool ok = mbar_wait<kCluster>(bar, parity, site, abort);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Byte offset of 16-byte chunk ch of row r in rows of `row_bytes` (a multiple
+// of 128): the low three chunk bits are XOR-ed with the row (bank spread).
+__device__ __forceinline__ uint32_t xrow_offset(uint32_t r, uint32_t ch, uint32_t row_bytes) {
+  return r * row_bytes + (((ch & ~7u) | ((ch ^ r) & 7u)) << 4);
 }
 
 // Pairwise (tree) max / sum of 32 values: log-depth dependency chains.
@@ -121,10 +139,12 @@ __device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
   return (a[0] + a[2]) + (a[1] + a[3]);
 }
 
-template <int kRC>
+template <int kRC, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_packed_kernel(const __grid_constant__ CUtensorMap mapQ,
-                        const __grid_constant__ CUtensorMap mapL, FlashArgs a) {
+                        const __grid_constant__ CUtensorMap mapL,
+                        const __grid_constant__ CUtensorMap mapWk,
+                        const __grid_constant__ CUtensorMap mapWv, FlashArgs a) {
   extern __shared__ uint8_t flash_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(flash_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,15 +160,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t peer = crank ^ 1u;
 
   // ---- work item: heavy row blocks first ----
+  // Head-packed rows: row = i*H + h of one batch entry (q' from the workspace).
+  // Fused prefill rows: row = query position i of one (batch entry, head).
   const int work = blockIdx.x / csize;
-  const int per_rb = a.B * a.splits;
+  const int per_rb = kFused ? a.B * a.H : a.B * a.splits;
   const int rb = a.row_blocks - 1 - work / per_rb;
-  const int b = (work / a.splits) % a.B;
-  const int sp = work % a.splits;
-  const int rows_b = a.Tq * a.H;
+  const int b = kFused ? (work % per_rb) / a.H : (work / a.splits) % a.B;
+  const int head = kFused ? work % a.H : 0;
+  const int sp = kFused ? 0 : work % a.splits;
+  const int rows_b = kFused ? a.Tq : a.Tq * a.H;
   const int row0 = rb * kRows;
   const int last_row = min(row0 + kRows, rows_b) - 1;
-  const int t_max = a.Tkv - a.Tq + last_row / a.H;
+  const int t_max = a.Tkv - a.Tq + (kFused ? last_row : last_row / a.H);
   const int kv_len = a.causal ? min(t_max + 1, a.Tkv) : a.Tkv;
   const int n_tiles_all = (kv_len + kKeys - 1) / kKeys;
   const int per_split = (n_tiles_all + a.splits - 1) / a.splits;
@@ -175,6 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->x_consumed[i], 8);  // one arrival per local softmax warp
     }
     mbar_init(&bars->o_last, 1);
+    mbar_init(&bars->pro_full, 1);
+    mbar_init(&bars->pro_done, 1);
+    mbar_init(&bars->epi_a, 256);
+    mbar_init(&bars->epi_w, 1);
+    mbar_init(&bars->epi_done, 1);
+    mbar_init(&bars->epi_x, 1);
     bars->abort_flag = 0;
     fence_mbarrier_init_cluster();
   }
@@ -190,9 +219,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && nt > 0) {
       prefetch_tensormap(&mapQ);
       prefetch_tensormap(&mapL);
-      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
-      for (int kc = 0; kc < nchunk; ++kc)
-        tma_load_3d(sP + kc * (kRows * 128), &mapQ, &bars->q_full, c0 + 64 * kc, row0, b);
+      if constexpr (kFused) {
+        // q tile (128 positions x d of one head) and this CTA's rows of w_up_k
+        // into latent stages 0-2; the latent ring starts once they are consumed.
+        const int dch = a.d / 64;
+        mbar_arrive_expect_tx(&bars->pro_full, (uint32_t)(kRows * a.d * 2 + RC * a.d * 2));
+        for (int kc = 0; kc < dch; ++kc) {
+          tma_load_3d(sL + kc * (kRows * 128), &mapQ, &bars->pro_full, 64 * kc, head,
+                      b * a.Tq + row0);
+          tma_load_3d(sL + kFusedWkOff + kc * (RC * 128), &mapWk, &bars->pro_full, 64 * kc, head,
+                      c0);
+        }
+        mbar_wait(&bars->pro_done, 0, 13, abort_flag);
+      } else {
+        mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
+        for (int kc = 0; kc < nchunk; ++kc)
+          tma_load_3d(sP + kc * (kRows * 128), &mapQ, &bars->q_full, c0 + 64 * kc, row0, b);
+      }
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int st = j % kStages;
@@ -207,7 +250,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Do not leave copies in flight: wait for the last loads of each stage.
       for (int j = max(0, issued - kStages); j < issued; ++j)
         mbar_wait(&bars->l_full[j % kStages], (j / kStages) & 1, 11, nullptr);
-      mbar_wait(&bars->q_full, 0, 12, nullptr);
+      if constexpr (kFused) {
+        // w_up_v rows of this CTA (MN-major B of the output MMA) once the last
+        // P.L has finished reading the latent stages
+        if (mbar_wait(&bars->o_last, 0, 14, abort_flag)) {
+          const int dch = a.d / 64;
+          mbar_arrive_expect_tx(&bars->epi_w, (uint32_t)(RC * a.d * 2));
+          for (int nc = 0; nc < dch; ++nc)
+            for (int kb = 0; kb < RC / 64; ++kb)
+              tma_load_3d(sL + kFusedWvOff + nc * (RC * 128) + kb * (64 * 128), &mapWv,
+                          &bars->epi_w, 64 * nc, head, c0 + 64 * kb);
+          mbar_wait(&bars->epi_w, 0, 15, nullptr);
+        }
+      } else {
+        mbar_wait(&bars->q_full, 0, 12, nullptr);
+      }
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
@@ -224,7 +281,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kSPerO = kSSteps / 4;          // S K-steps per O K-step
       const uint32_t l0 = smem_u32(sL), p0 = smem_u32(sP);
       const uint32_t tq = tmem + kTmemQ;
-      bool ok = mbar_wait(&bars->q_ready, 0, 20, abort_flag);
+      bool ok = true;
+      if constexpr (kFused) {
+        // q' (fp32, this CTA's rank columns) = q . w_up_k[:, h, c0:c0+RC]^T into O's columns
+        ok = mbar_wait(&bars->pro_full, 0, 24, abort_flag);
+        tc_fence_after();
+        if (ok) {
+          constexpr uint32_t idesc_q = make_idesc_bf16(kRows, kRC, false, false);
+          const uint64_t aq = make_sdesc_sw128(l0, 16, 1024);
+          const uint64_t bw = make_sdesc_sw128(l0 + kFusedWkOff, 16, 1024);
+          for (int k = 0; k < a.d / 16; ++k)
+            umma_bf16(tmem + kTmemO, aq + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
+                      bw + (uint64_t)(((k >> 2) * (kRC * 128) + (k & 3) * 32) >> 4), idesc_q,
+                      k > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->pro_done);
+      }
+      ok = ok && mbar_wait(&bars->q_ready, 0, 20, abort_flag);
       tc_fence_after();
       // S K-step k of a tile: A = q' columns [8k, 8k+8) of TMEM, B = latent K-chunk k/4
 #define MLA_S_STEP(sbuf, bd, k)                                                          \
@@ -287,6 +360,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #undef MLA_S_STEP
       umma_commit(&bars->o_last);
+      if constexpr (kFused) {
+        // out_partial = O_lat(bf16, smem) . w_up_v[c0:c0+RC, h, :] into S's columns
+        if (ok && mbar_wait(&bars->epi_a, 0, 25, abort_flag) &&
+            mbar_wait(&bars->epi_w, 0, 26, abort_flag)) {
+          tc_fence_after();
+          const uint32_t idesc_v = make_idesc_bf16(kRows, a.d, false, true);
+          const uint64_t ao = make_sdesc_sw128(l0, 16, 1024);
+          const uint64_t bv = make_sdesc_sw128(l0 + kFusedWvOff, kRC * 128, 1024);
+#pragma unroll
+          for (int k = 0; k < kRC / 16; ++k)
+            umma_bf16(tmem + kTmemS, ao + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
+                      bv + (uint64_t)((k * 2048) >> 4), idesc_v, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->epi_done);
+      }
     }
   } else if (warp < 6) {
     // ======================= partial-S exchange (CTA pair) =======================
@@ -319,6 +407,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars->s_empty[bi]);
       }
+      if constexpr (kFused) {
+        // send the peer the half of this CTA's partial output that the peer stores,
+        // once the peer's receive buffers are free (their last release)
+        const int dh = a.d / 2;
+        const int send0 = (int)peer * dh;
+        bool okx = warp_wait(&bars->epi_done, 0, 42, abort_flag);
+        okx = okx && warp_wait<true>(&bars->x_empty[0], ((nt + 1) / 2) & 1, 43, abort_flag);
+        okx = okx && warp_wait<true>(&bars->x_empty[1], (nt / 2) & 1, 44, abort_flag);
+        if (okx) {
+          tc_fence_after();
+          const uint32_t epx_peer = mapa_shared(smem_u32(&bars->epi_x), peer);
+          for (int c = 0; c < dh; c += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + kTmemS + send0 + c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_async_v4(x_peer0 + xrow_offset(r, (uint32_t)((c >> 2) + q), (uint32_t)(dh * 4)),
+                          v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], epx_peer);
+          }
+        }
+      }
     }
   } else if (warp == 14) {
     // ======================= release forwarding (CTA pair) =======================
@@ -345,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = qd * 32 + lane;                 // row within the tile
     const int grow = row0 + r;                    // row within batch entry b
     const bool row_valid = grow < rows_b;
-    const int t_row = a.Tkv - a.Tq + (row_valid ? grow / a.H : 0);
+    const int t_row = a.Tkv - a.Tq + (row_valid ? (kFused ? grow : grow / a.H) : 0);
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const uint32_t x_local = smem_u32(sX);
     float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2][128] partner exchange
@@ -355,6 +465,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_half = 0.f;
     bool ok = nt > 0;
     if (ok) {
+      if constexpr (kFused) {
+        // q' (fp32 in O's columns) -> scaled by scale*log2(e) -> bf16 pairs in TMEM
+        ok = warp_wait(&bars->pro_done, 0, 28, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          for (int c = oc0; c < oc0 + RC / 2; c += 32) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + kTmemO + c, v);
+            tmem_wait_ld();
+            float pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = __uint_as_float(pack_bf16x2(v[2 * e] * a.qscale, v[2 * e + 1] * a.qscale));
+            tmem_st16(tmem + lane_base + kTmemQ + c / 2, pk);
+          }
+          if (a.pair && warp == 6 && lane == 0)
+            mbar_arrive_expect_tx(&bars->epi_x, (uint32_t)(kRows * (a.d / 2) * 4));
+        }
+      } else {
       // q' (staged by TMA in the receive buffers, 128-byte swizzled rows) -> TMEM
       ok = warp_wait(&bars->q_full, 0, 29, abort_flag);
       if (ok) {
@@ -374,6 +503,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : "memory");
           }
         }
+      }
+      }
+      if (ok) {
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->q_ready);
@@ -495,9 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       have_o = warp_wait(&bars->o_last, 0, 35, abort_flag);
       tc_fence_after();
     }
-    if (a.splits == 1) {
+    if constexpr (kFused) {
+      // normalised O_lat (bf16) -> shared memory, the A operand of the output MMA
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.olat) + gr * a.R + c0;
+      const uint32_t a0s = smem_u32(sL);
       for (int c = oc0; c < oc0 + RC / 2; c += 32) {
         float o[32];
         if (have_o) {
@@ -507,38 +640,111 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0.f;
         }
-        if (row_valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+        const uint32_t base = a0s + (uint32_t)(c >> 6) * (kRows * 128);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            d4[q] = make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
-                               pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                               pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                               pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+        for (int q = 0; q < 4; ++q)
+          st_shared_v4(base + sw128_offset((uint32_t)r, (uint32_t)(((c & 63) >> 3) + q)),
+                       pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                       pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                       pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                       pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->epi_a);
+      // out[b, i, h, :] = O_lat . w_up_v[:, h, :]; a CTA pair adds the peer's
+      // partial product for the half of the columns this CTA stores
+      bool have_out = have_o && warp_wait(&bars->epi_done, 0, 36, abort_flag);
+      tc_fence_after();
+      const int dh = a.pair ? a.d / 2 : a.d;                 // columns stored by this CTA
+      const int cfirst = (a.pair ? (int)crank * dh : 0) + half * (dh / 2);
+      bool have_peer = true;
+      if (a.pair) have_peer = have_out && warp_wait<true>(&bars->epi_x, 0, 37, abort_flag);
+      const int64_t orow = (((int64_t)b * a.Tq + grow) * a.H + head) * a.d;
+      for (int c = cfirst; c < cfirst + dh / 2; c += 16) {
+        float v[16];
+        if (have_out) {
+          tmem_ld16(tmem + lane_base + kTmemS + c, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = 0.f;
+        }
+        if (a.pair && have_peer) {
+          const int cc = c - (int)crank * dh;          // column within the received half
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float x0, x1, x2, x3;
+            ld_shared_v4f(x_local + xrow_offset((uint32_t)r, (uint32_t)((cc >> 2) + q),
+                                                (uint32_t)(dh * 4)),
+                          x0, x1, x2, x3);
+            v[4 * q] += x0;
+            v[4 * q + 1] += x1;
+            v[4 * q + 2] += x2;
+            v[4 * q + 3] += x3;
+          }
+        }
+        if (row_valid && have_peer) {
+          if (a.out_bf16) {
+            uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + c);
+            d4[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+            d4[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
+                               pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
+          } else {
+            float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          }
         }
       }
     } else {
-      float* dst = a.part_o + ((int64_t)sp * nrows + gr) * a.R + c0;
-      for (int c = oc0; c < oc0 + RC / 2; c += 32) {
-        float o[32];
-        if (have_o) {
-          tmem_ld32(tmem + lane_base + kTmemO + c, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      if (a.splits == 1) {
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.olat) + gr * a.R + c0;
+        for (int c = oc0; c < oc0 + RC / 2; c += 32) {
+          float o[32];
+          if (have_o) {
+            tmem_ld32(tmem + lane_base + kTmemO + c, o);
+            tmem_wait_ld();
+          } else {
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0.f;
+          }
+          if (row_valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+  #pragma unroll
+            for (int q = 0; q < 4; ++q)
+              d4[q] = make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                 pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                 pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                 pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+          }
         }
-        if (row_valid) {
-          float4* d4 = reinterpret_cast<float4*>(dst + c);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            d4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      } else {
+        float* dst = a.part_o + ((int64_t)sp * nrows + gr) * a.R + c0;
+        for (int c = oc0; c < oc0 + RC / 2; c += 32) {
+          float o[32];
+          if (have_o) {
+            tmem_ld32(tmem + lane_base + kTmemO + c, o);
+            tmem_wait_ld();
+          } else {
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0.f;
+          }
+          if (row_valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c);
+  #pragma unroll
+            for (int q = 0; q < 8; ++q)
+              d4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          }
         }
-      }
-      if (row_valid && crank == 0 && half == 0) {
-        float* ml = a.part_ml + ((int64_t)sp * nrows + gr) * 2;
-        ml[0] = have_o ? m_run : -INFINITY;
-        ml[1] = have_o ? l_run : 0.f;
+        if (row_valid && crank == 0 && half == 0) {
+          float* ml = a.part_ml + ((int64_t)sp * nrows + gr) * 2;
+          ml[0] = have_o ? m_run : -INFINITY;
+          ml[1] = have_o ? l_run : 0.f;
+        }
       }
     }
   }
@@ -596,15 +802,17 @@ __global__ void merge_partials_kernel(const float* __restrict__ ml, int ml_strid
 
 }  // namespace
 
-template <int kRC>
+template <int kRC, bool kFused>
 static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                  const CUtensorMap& mapWk, const CUtensorMap& mapWv,
                                   const FlashArgs& args, cudaStream_t stream) {
-  auto kern = flash_packed_kernel<kRC>;
+  auto kern = flash_packed_kernel<kRC, kFused>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int csize = args.pair ? 2 : 1;
-  const unsigned blocks = (unsigned)(args.row_blocks * args.B * args.splits * csize);
+  const int per_rb = kFused ? args.B * args.H : args.B * args.splits;
+  const unsigned blocks = (unsigned)(args.row_blocks * per_rb * csize);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -617,7 +825,7 @@ static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& m
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, args);
+  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -625,10 +833,22 @@ static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& m
 cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                 const FlashArgs& args, cudaStream_t stream) {
   switch (args.RC) {
-    case 64: return launch_flash_rc<64>(mapQ, mapL, args, stream);
-    case 128: return launch_flash_rc<128>(mapQ, mapL, args, stream);
-    case 192: return launch_flash_rc<192>(mapQ, mapL, args, stream);
-    case 256: return launch_flash_rc<256>(mapQ, mapL, args, stream);
+    case 64: return launch_flash_rc<64, false>(mapQ, mapL, mapQ, mapQ, args, stream);
+    case 128: return launch_flash_rc<128, false>(mapQ, mapL, mapQ, mapQ, args, stream);
+    case 192: return launch_flash_rc<192, false>(mapQ, mapL, mapQ, mapQ, args, stream);
+    case 256: return launch_flash_rc<256, false>(mapQ, mapL, mapQ, mapQ, args, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                               const CUtensorMap& mapWk, const CUtensorMap& mapWv,
+                               const FlashArgs& args, cudaStream_t stream) {
+  switch (args.RC) {
+    case 64: return launch_flash_rc<64, true>(mapQ, mapL, mapWk, mapWv, args, stream);
+    case 128: return launch_flash_rc<128, true>(mapQ, mapL, mapWk, mapWv, args, stream);
+    case 192: return launch_flash_rc<192, true>(mapQ, mapL, mapWk, mapWv, args, stream);
+    case 256: return launch_flash_rc<256, true>(mapQ, mapL, mapWk, mapWv, args, stream);
     default: return cudaErrorInvalidValue;
   }
 }

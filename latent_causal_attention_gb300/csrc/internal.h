@@ -48,12 +48,24 @@ struct FlashArgs {
   int row_blocks;    // ceil(Tq*H / 128)
   int splits;        // key-range partitions
   int causal;
+  // fused prefill (rows = query positions of one head): q and the weights are
+  // read directly, out (B,Tq,H,d) written; no workspace
+  int d;
+  float qscale;      // scale * log2(e), applied to q' before rounding to bf16
+  void* out;
+  int out_bf16;
   void* olat;        // splits == 1: normalised latent-space output, bf16 (B*Tq*H, R)
   float* part_o;     // splits > 1: (splits, B*Tq*H, R) unnormalised
   float* part_ml;    // splits > 1: (splits, B*Tq*H, 2) = (max in log2 units, sum)
 };
 cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                 const FlashArgs& args, cudaStream_t stream);
+
+// Fused prefill: q (3-D map {d, H, B*Tq}, box {64,1,128}), latent, w_up_k
+// (K-major, {d, H, R}, box {64,1,RC}), w_up_v (MN-major, {d, H, R}, box {64,1,64}).
+cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                               const CUtensorMap& mapWk, const CUtensorMap& mapWv,
+                               const FlashArgs& args, cudaStream_t stream);
 
 cudaError_t launch_merge_partials(const float* m_l, int ml_stride, const float* l, const float* o,
                                   void* out, int parts, int rows, int width, int out_bf16,

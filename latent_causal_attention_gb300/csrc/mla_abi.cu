@@ -58,6 +58,7 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t d
 // ---------------------------------------------------------------------------
 static int g_attn_path = 0;     // 0 auto, 1 warp, 2 tensor core
 static int g_kv_splits = 0;     // 0 auto
+static int g_prefill_fused = 1; // 1: one fused kernel per head for long prefill
 static void** g_stage_events = nullptr;
 static int g_stage_events_n = 0;
 static unsigned long long g_launches = 0;
@@ -92,6 +93,7 @@ static int pick_bn(int N) {
 // ---------------------------------------------------------------------------
 struct AttnPlan {
   bool tc;
+  bool fused;             // per-head fused kernel (no workspace)
   int pair, RC, row_blocks, splits;
   int64_t rows;           // B*Tq*H
   size_t off_qp, off_olat, off_po, off_pml, total;
@@ -115,6 +117,15 @@ static AttnPlan plan_attention(int B, int Tq, int Tkv, int H, int d, int R, int 
   p.pair = R > 256 ? 1 : 0;
   p.RC = p.pair ? R / 2 : R;
   p.rows = (int64_t)B * Tq * H;
+  // Long prefill: rows are 128 query positions of one head, so the kernel can
+  // absorb w_up_k and apply w_up_v itself; needs d <= 128 for its staging.
+  p.fused = g_prefill_fused && g_kv_splits == 0 && Tq >= 64 && d <= 128;
+  if (p.fused) {
+    p.row_blocks = (Tq + 127) / 128;
+    p.splits = 1;
+    p.total = 0;
+    return p;
+  }
   p.row_blocks = (int)((int64_t)Tq * H + 127) / 128;
   const int csize = p.pair ? 2 : 1;
   const int64_t ctas = (int64_t)p.row_blocks * B * csize;
@@ -172,6 +183,10 @@ mla_status_t mla_set_option(int option, int64_t value) {
     case MLA_OPT_KV_SPLITS:
       if (value < 0 || value > 4096) return MLA_ERR_SHAPE;
       g_kv_splits = (int)value;
+      return MLA_OK;
+    case MLA_OPT_PREFILL_FUSED:
+      if (value < 0 || value > 1) return MLA_ERR_SHAPE;
+      g_prefill_fused = (int)value;
       return MLA_OK;
     default:
       return MLA_ERR_UNSUPPORTED;
@@ -301,6 +316,30 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
                                    stream);
     }));
   }
+  const int R = rank;
+  const int64_t BT = (int64_t)B * Tq;
+  if (p.fused) {
+    // one kernel: q . w_up_k -> flash loop over the latent -> . w_up_v -> out
+    CUtensorMap mQ, mL, mWk, mWv;
+    if (!make_tmap_3d(&mQ, q, 2, d, H, BT, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 128,
+                      true) ||
+        !make_tmap_3d(&mL, kv_latent, 2, R, Tkv, B, (uint64_t)R * 2, (uint64_t)Tkv * R * 2, 64, 64,
+                      1, true) ||
+        !make_tmap_3d(&mWk, w_up_k, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1,
+                      p.RC, true) ||
+        !make_tmap_3d(&mWv, w_up_v, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 64,
+                      true))
+      return MLA_ERR_CUDA;
+    FlashArgs fa = {};
+    fa.B = B; fa.Tq = Tq; fa.Tkv = Tkv; fa.H = H; fa.R = R; fa.RC = p.RC; fa.pair = p.pair;
+    fa.row_blocks = p.row_blocks; fa.splits = 1; fa.causal = causal ? 1 : 0;
+    fa.d = d; fa.qscale = scale * 1.4426950408889634f; fa.out = out;
+    fa.out_bf16 = out_dtype == MLA_BF16;
+    if (staged(1, stream, [&] { return launch_flash_fused(mQ, mL, mWk, mWv, fa, stream); }) !=
+        cudaSuccess)
+      return MLA_ERR_CUDA;
+    return MLA_OK;
+  }
   if (!workspace) return MLA_ERR_WORKSPACE;
   if (workspace_bytes < p.total) return MLA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLA_ERR_ALIGN;
@@ -308,8 +347,6 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* qp = ws + p.off_qp;
   void* olat = ws + p.off_olat;
-  const int R = rank;
-  const int64_t BT = (int64_t)B * Tq;
 
   // 1. absorption: q'[(b,i), h, :] = scale*log2(e) * w_up_k[:, h, :] q[(b,i), h, :]
   CUtensorMap mA, mB;

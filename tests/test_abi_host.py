@@ -76,7 +76,13 @@ def test_workspace_size_rules(lib):
     ws = lib.mla_latent_attention_workspace_size
     assert ws(2, 32, 32, 4, 16, 24, 0, 1) == 0                 # fp32: warp path, no workspace
     assert ws(2, 32, 32, 4, 16, 24, 1, 1) == 0                 # bf16, d=16: warp path
-    assert ws(4, 1024, 1024, 16, 64, 256, 1, 1) >= 2 * 4 * 1024 * 16 * 256 * 2
+    assert ws(4, 1024, 1024, 16, 64, 256, 1, 1) == 0           # fused prefill kernel: none
+    assert lib.mla_set_option(_lib.OPT_PREFILL_FUSED, 0) == 0
+    try:                                                        # head-packed kernels
+        assert ws(4, 1024, 1024, 16, 64, 256, 1, 1) >= 2 * 4 * 1024 * 16 * 256 * 2
+    finally:
+        lib.mla_set_option(_lib.OPT_PREFILL_FUSED, 1)
+    assert ws(4, 1024, 1024, 16, 192, 256, 1, 1) > 0            # d > 128: head-packed
     assert ws(0, 1, 1, 1, 64, 64, 1, 1) == 0
     # forcing several key partitions adds the partial buffers
     base = ws(64, 1, 4096, 128, 128, 512, 1, 1)

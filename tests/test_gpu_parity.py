@@ -28,6 +28,7 @@ def _built():
     build()
     mla.set_option(_lib.OPT_ATTN_PATH, 0)
     mla.set_option(_lib.OPT_KV_SPLITS, 0)
+    mla.set_option(_lib.OPT_PREFILL_FUSED, 1)
     yield
     assert mla.device_error() == 0
 
@@ -162,22 +163,28 @@ EDGE = [
 ]
 
 
+MODES = {"auto": (0, 1), "packed": (0, 0), "split3": (3, 1)}   # (kv splits, prefill fused)
+
+
 @pytest.mark.parametrize("shape", EDGE, ids=lambda s: "x".join(str(v) for v in s.values()))
-@pytest.mark.parametrize("splits", [0, 3])
-def test_tensor_core_path_edges(oracle, shape, splits):
+@pytest.mark.parametrize("mode", list(MODES))
+def test_tensor_core_path_edges(oracle, shape, mode):
+    """Auto (fused per-head prefill kernel when Tq >= 64 and d <= 128, else the
+    head-packed kernels), the head-packed kernels forced, and split-KV forced."""
     w = custom_workload("edge", dtype="bf16", **shape)
     x = make_inputs(w, seed=11)
+    splits, fused = MODES[mode]
     mla.set_option(_lib.OPT_KV_SPLITS, splits)
+    mla.set_option(_lib.OPT_PREFILL_FUSED, fused)
     try:
-        assert mla.workspace_size(w.B, w.Tq, w.Tkv, w.H, w.d, w.rank, torch.bfloat16,
-                                  w.causal) > 0
         out = run_attention(x, w)
         outb = run_attention(x, w, out_dtype=torch.bfloat16)
     finally:
         mla.set_option(_lib.OPT_KV_SPLITS, 0)
+        mla.set_option(_lib.OPT_PREFILL_FUSED, 1)
     ref = oracle.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale, w.causal)
-    assert_bf16_close(out, ref, f"{shape} splits={splits}")
-    assert_bf16_close(outb.float(), ref, f"{shape} splits={splits} bf16 out")
+    assert_bf16_close(out, ref, f"{shape} {mode}")
+    assert_bf16_close(outb.float(), ref, f"{shape} {mode} bf16 out")
 
 
 def test_bf16_small_head_takes_warp_path(oracle):

@@ -35,6 +35,7 @@ def lib():
     lib = _lib.load()
     mla.set_option(_lib.OPT_ATTN_PATH, 0)
     mla.set_option(_lib.OPT_KV_SPLITS, 0)
+    mla.set_option(_lib.OPT_PREFILL_FUSED, 1)
     return lib
 
 
@@ -76,8 +77,9 @@ def test_noalloc_matches_regular_entry_point(lib, w):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
-    """The prefill workload needs ~0.5 GB of scratch: refused, nothing launched."""
-    w = WORKLOADS["prefill_bf16"]
+    """A decode batch with 32 queries per sequence over 4096 positions, 128
+    heads, rank 512 needs ~67 MB of scratch: refused, nothing launched."""
+    w = custom_workload("big", dtype="bf16", B=8, Tq=32, Tkv=4096, H=128, d=128, rank=512)
     need = mla.workspace_size(w.B, w.Tq, w.Tkv, w.H, w.d, w.rank, torch.bfloat16)
     assert need > 32 * 1024 * 1024
     dummy = ctypes.c_void_p(256)            # never dereferenced: the size check comes first
