@@ -47,7 +47,8 @@ namespace {
 
 constexpr int kRows = 128;           // rows per CTA tile (MMA M)
 constexpr int kKeys = 64;            // keys per tile (S MMA N, O MMA K)
-constexpr int kStages = 5;           // latent tile ring
+constexpr int kStages = 4;           // latent tile ring
+constexpr int kXBuf = 4;             // receive buffers of partial S (CTA pair)
 constexpr int kMaxRC = 256;          // rank columns per CTA
 constexpr int kThreads = 480;          // 15 warps
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
@@ -58,9 +59,11 @@ constexpr int kXBytes = kRows * kKeys * 2;        // 16 KB per receive buffer (f
 constexpr int kOffL = 0;
 constexpr int kOffP = kOffL + kStages * kLStage;  // P and receive buffers: staging of q' (64 KB)
 constexpr int kOffX = kOffP + 2 * kPBytes;
-constexpr int kOffRed = kOffX + 2 * kXBytes;      // 2 x 128 floats: softmax warp-pair exchange
+constexpr int kOffRed = kOffX + kXBuf * kXBytes;  // 2 x 128 floats: softmax warp-pair exchange
 constexpr int kOffBar = kOffRed + 1024;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;   // + barriers + alignment slack
+constexpr int kBarBytes = 512;
+constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + barriers + alignment slack
+static_assert(kSmemBytes <= 232448, "dynamic shared memory limit");
 
 // fused prefill staging inside the latent ring (before / after the loop):
 //   prologue: q tile at 0 (d/64 x 16 KB), w_up_k rows at 32 KB (d/64 x RC*128 B)
@@ -82,9 +85,9 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t p_empty[2];
   uint64_t o_last;
-  uint64_t x_full[2];          // my receive buffer b was filled by the peer
-  uint64_t x_empty[2];         // the peer's receive buffer b may be written again
-  uint64_t x_consumed[2];      // my softmax warps are done with my receive buffer b
+  uint64_t x_full[kXBuf];      // my receive buffer b was filled by the peer
+  uint64_t x_empty[kXBuf];     // the peer's receive buffer b may be written again
+  uint64_t x_consumed[kXBuf];  // my softmax warps are done with my receive buffer b
   uint64_t pro_full;           // fused prefill: q tile and w_up_k staged (TMA)
   uint64_t pro_done;           // fused prefill: q . w_up_k^T computed into TMEM
   uint64_t epi_a;              // fused prefill: normalised O_lat (bf16) written to smem
@@ -94,6 +97,8 @@ struct Bars {
   uint32_t tmem_slot;
   int abort_flag;
 };
+
+static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -193,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_empty[i], a.pair ? 384 : 256);
       mbar_init(&bars->p_full[i], 256);
       mbar_init(&bars->p_empty[i], 1);
+    }
+    for (int i = 0; i < kXBuf; ++i) {
       mbar_init(&bars->x_full[i], 1);      // armed by one local thread; bytes from the peer
       mbar_init(&bars->x_empty[i], 1);     // forwarded by the peer's forwarding warp
       mbar_init(&bars->x_consumed[i], 8);  // one arrival per local softmax warp
@@ -384,14 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
       const uint32_t x_peer0 = mapa_shared(smem_u32(sX), peer);
       const uint32_t xfull_peer0 = mapa_shared(smem_u32(&bars->x_full[0]), peer);
-      const uint32_t xfull_peer1 = mapa_shared(smem_u32(&bars->x_full[1]), peer);
       for (int j = 0; j < nt; ++j) {
-        const int bi = j & 1, k = j >> 1;
+        const int bi = j & 1, k = j >> 1;                 // S buffer and its use count
+        const int xb = j % kXBuf, xk = j / kXBuf;         // receive buffer and its use count
         if (!warp_wait(&bars->s_full[bi], k & 1, 40, abort_flag)) break;
         tc_fence_after();
-        if (!warp_wait<true>(&bars->x_empty[bi], k & 1, 41, abort_flag)) break;
-        const uint32_t dst = x_peer0 + bi * kXBytes;
-        const uint32_t bar = bi ? xfull_peer1 : xfull_peer0;
+        if (!warp_wait<true>(&bars->x_empty[xb], xk & 1, 41, abort_flag)) break;
+        const uint32_t dst = x_peer0 + xb * kXBytes;
+        const uint32_t bar = xfull_peer0 + xb * 8;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {          // two 32-column halves, sent as fp16
           float v[32];
@@ -413,8 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int dh = a.d / 2;
         const int send0 = (int)peer * dh;
         bool okx = warp_wait(&bars->epi_done, 0, 42, abort_flag);
-        okx = okx && warp_wait<true>(&bars->x_empty[0], ((nt + 1) / 2) & 1, 43, abort_flag);
-        okx = okx && warp_wait<true>(&bars->x_empty[1], (nt / 2) & 1, 44, abort_flag);
+        for (int xb = 0; xb < kXBuf; ++xb)          // last release of each receive buffer
+          okx = okx && warp_wait<true>(&bars->x_empty[xb], ((nt - xb + kXBuf - 1) / kXBuf) & 1,
+                                       43, abort_flag);
         if (okx) {
           tc_fence_after();
           const uint32_t epx_peer = mapa_shared(smem_u32(&bars->epi_x), peer);
@@ -433,17 +441,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 14) {
     // ======================= release forwarding (CTA pair) =======================
     // Passes "my receive buffer b is free" from the local softmax warps to the
-    // peer's x_empty[b]: the initial release of both buffers, then one per tile.
+    // peer's x_empty[b]: the initial release of every buffer, then one per tile.
     // The cluster-scope arrival is a round trip; keeping it on this warp keeps
     // it off the softmax warps' path.
     if (a.pair && nt > 0 && lane == 0) {
       const uint32_t xe_peer0 = mapa_shared(smem_u32(&bars->x_empty[0]), peer);
-      const uint32_t xe_peer1 = mapa_shared(smem_u32(&bars->x_empty[1]), peer);
-      for (int n = 0; n < nt + 2; ++n) {
-        const int bi = n < 2 ? n : (n - 2) & 1;
-        const int ph = n < 2 ? 0 : ((n - 2) >> 1) + 1;     // completion index of x_consumed[bi]
-        if (!mbar_wait(&bars->x_consumed[bi], ph & 1, 45, abort_flag)) break;
-        mbar_arrive_remote(bi ? xe_peer1 : xe_peer0);
+      for (int n = 0; n < nt + kXBuf; ++n) {
+        // n < kXBuf: the initial release of buffer n; then tile j = n - kXBuf
+        const int xb = n < kXBuf ? n : (n - kXBuf) % kXBuf;
+        const int ph = n < kXBuf ? 0 : (n - kXBuf) / kXBuf + 1;   // completion index
+        if (!mbar_wait(&bars->x_consumed[xb], ph & 1, 45, abort_flag)) break;
+        mbar_arrive_remote(xe_peer0 + xb * 8);
       }
     }
   } else {
@@ -510,17 +518,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars->q_ready);
         if (a.pair) {                 // my receive buffers may now be written by the peer
-          if (warp == 6 && lane == 0) {   // arm the receive barriers of tiles 0 and 1
-            mbar_arrive_expect_tx(&bars->x_full[0], (uint32_t)kXBytes);
-            if (nt > 1) mbar_arrive_expect_tx(&bars->x_full[1], (uint32_t)kXBytes);
-          }
+          if (warp == 6 && lane == 0)     // arm the receive barriers of the first tiles
+            for (int xb = 0; xb < kXBuf && xb < nt; ++xb)
+              mbar_arrive_expect_tx(&bars->x_full[xb], (uint32_t)kXBytes);
           // every lane's reads are consumed before __syncwarp; the forwarding
           // warp passes the release on to the peer
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bars->x_consumed[0]);
-            mbar_arrive(&bars->x_consumed[1]);
-          }
+          if (lane == 0)
+            for (int xb = 0; xb < kXBuf; ++xb) mbar_arrive(&bars->x_consumed[xb]);
         }
       }
     }
@@ -536,8 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (a.pair) {
         // the peer's partial S over its half of the rank (my 32 keys)
-        if (!warp_wait<true>(&bars->x_full[bi], k & 1, 32, abort_flag)) { ok = false; break; }
-        const uint32_t src = x_local + bi * kXBytes;
+        const int xb = j % kXBuf, xk = j / kXBuf;
+        if (!warp_wait<true>(&bars->x_full[xb], xk & 1, 32, abort_flag)) { ok = false; break; }
+        const uint32_t src = x_local + xb * kXBytes;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t u0, u1, u2, u3;
@@ -552,11 +558,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           s[8 * c + 4] += f2.x; s[8 * c + 5] += f2.y;
           s[8 * c + 6] += f3.x; s[8 * c + 7] += f3.y;
         }
-        // re-arm this buffer's barrier for tile j+2 (its phase for tile j is complete)
-        if (warp == 6 && lane == 0 && j + 2 < nt)
-          mbar_arrive_expect_tx(&bars->x_full[bi], (uint32_t)kXBytes);
+        // re-arm this buffer's barrier for tile j+kXBuf (its phase for tile j is complete)
+        if (warp == 6 && lane == 0 && j + kXBuf < nt)
+          mbar_arrive_expect_tx(&bars->x_full[xb], (uint32_t)kXBytes);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->x_consumed[bi]);
+        if (lane == 0) mbar_arrive(&bars->x_consumed[xb]);
       }
 
       // mask: key s_idx visible iff s_idx < Tkv and (not causal or s_idx <= t)
