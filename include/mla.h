@@ -190,6 +190,15 @@ mla_status_t mla_merge_partials(const float* m, const float* l, const float* o, 
  */
 mla_status_t mla_get_device_error(unsigned int* code, int clear);
 
+/*
+ * Exercises the bounded-wait path without touching any data: launches one
+ * kernel whose mbarrier wait can never complete, bounded by limit_us
+ * microseconds (1 .. 10^7).  When it runs out the kernel records the timeout
+ * (kernel-side code 0x17f) in the device error word read by
+ * mla_get_device_error and returns; the context stays usable.
+ */
+mla_status_t mla_check_wait_timeout(unsigned int limit_us, void* stream);
+
 /* Process-global tuning switches (not thread-safe; for tests and tuning). */
 typedef enum {
   MLA_OPT_ATTN_PATH = 0,       /* 0 auto, 1 force warp path, 2 force tensor-core path */

@@ -32,6 +32,7 @@ SIGNATURES = {
     "mla_status_string": (ctypes.c_char_p, [_i]),
     "mla_set_stage_events": (_i, [ctypes.POINTER(ctypes.c_void_p), _i]),
     "mla_launch_count": (ctypes.c_uint64, []),
+    "mla_check_wait_timeout": (_i, [ctypes.c_uint, _vp]),
 }
 
 

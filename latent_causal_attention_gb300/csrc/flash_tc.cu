@@ -806,7 +806,30 @@ __global__ void merge_partials_kernel(const float* __restrict__ ml, int ml_strid
   }
 }
 
+// Bounded-wait check: one thread waits on an mbarrier that nothing arrives on,
+// with a caller-chosen limit, records kErrWaitTimeout | 0x7f and returns -- the
+// same path every wait in the kernels above takes when it runs out of time.
+__global__ void wait_timeout_probe_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbarrier_init_cluster();
+  const uint32_t a = smem_u32(&bar);
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, 0)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      report_error(kErrWaitTimeout | 0x7fu);
+      return;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
+}
 
 template <int kRC, bool kFused>
 static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& mapL,

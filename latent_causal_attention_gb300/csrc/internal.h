@@ -71,6 +71,9 @@ cudaError_t launch_merge_partials(const float* m_l, int ml_stride, const float* 
                                   void* out, int parts, int rows, int width, int out_bf16,
                                   cudaStream_t stream);
 
+// Launches a kernel whose only wait can never complete, bounded by limit_ns.
+cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, cudaStream_t stream);
+
 // Device-side error words (one per translation unit with bounded waits).
 cudaError_t gemm_read_device_error(unsigned int* code, int clear);
 cudaError_t flash_read_device_error(unsigned int* code, int clear);

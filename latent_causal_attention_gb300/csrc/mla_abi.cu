@@ -200,6 +200,12 @@ mla_status_t mla_set_stage_events(void** events, int n) {
   return MLA_OK;
 }
 
+mla_status_t mla_check_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 10u * 1000u * 1000u) return MLA_ERR_SHAPE;
+  return cuda_status(launch_wait_timeout_probe((unsigned long long)limit_us * 1000ull,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 uint64_t mla_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
 
 mla_status_t mla_get_device_error(unsigned int* code, int clear) {

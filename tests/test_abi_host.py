@@ -101,6 +101,11 @@ def test_project_validation(lib):
     assert f(P, P, None, None, P, None, None, 8, 64, 64, 0, 0, 1, None) == 3
 
 
+def test_wait_check_validation(lib):
+    assert lib.mla_check_wait_timeout(0, None) == 2
+    assert lib.mla_check_wait_timeout(20_000_000, None) == 2
+
+
 def test_options(lib):
     assert lib.mla_set_option(0, 3) == 2
     assert lib.mla_set_option(99, 0) == 8

@@ -239,3 +239,16 @@ def test_merge_random_against_oracle(oracle):
     for r in range(rows):
         ref = oracle.merge_partials(m32[:, r] * ln2, l32[:, r], o32[:, r])
         assert_f32_close(to_np(out)[r], ref, f"row {r}")
+
+
+# ----------------------------------------------------------------- failure detection
+def test_bounded_wait_reports_timeout_and_context_survives(oracle):
+    """A wait that can never complete runs out after its limit, records the
+    timeout in the device error word and returns; later work still runs."""
+    lib = _lib.load()
+    assert mla.device_error(clear=True) == 0
+    assert lib.mla_check_wait_timeout(2000, None) == 0          # 2 ms limit
+    torch.cuda.synchronize()
+    assert mla.device_error(clear=True) == 0x17F
+    assert mla.device_error() == 0
+    test_tiny_f32_full(oracle)                                  # the context is still usable
