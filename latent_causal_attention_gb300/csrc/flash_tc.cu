@@ -25,16 +25,19 @@
 // cluster split the rank: each holds q', the latent tiles and O_lat for its
 // half and computes a partial S over its half; dedicated exchange warps send
 // each partial S tile to the peer through distributed shared memory one step
-// ahead of the softmax (double-buffered receive buffers).  Both CTAs then run
-// the identical softmax (a + b is the same bits in either CTA) and accumulate
-// their half of O_lat.
+// ahead of the softmax (four receive buffers).  The partial S travels as fp16;
+// each CTA adds the peer's fp16 partial to its own fp32 partial, runs the
+// softmax over the 128 x 64 tile and accumulates its half of O_lat with its own
+// running max and sum (the two CTAs' logits differ only by the fp16 rounding of
+// the partial each receives).
 //
-// Warp roles (480 threads): warp 0 lane 0 = TMA producer (q' once, then a
-// 4-stage ring of latent tiles); warp 1 = TMEM owner, lane 0 issues MMAs;
-// warps 2-5 = partial-S exchange (CTA pair only); warps 6-13 = softmax and
-// epilogue, two warps per row quadrant (each takes 32 of a tile's 64 keys and
-// half of O_lat's columns); warp 14 forwards receive-buffer releases to the
-// peer (CTA pair only).  Warp w reads TMEM lanes 32*(w%4)..+31.
+// Warp roles (512 threads): warp 0 lane 0 = TMA producer (q' once, then a
+// 4-stage ring of latent tiles); warp 1 = TMEM owner, lane 0 issues the MMAs of
+// even tiles; warp 15 lane 0 issues those of odd tiles; warps 2-5 = partial-S
+// exchange (CTA pair only); warps 6-13 = softmax and epilogue, two warps per
+// row quadrant (each takes 32 of a tile's 64 keys and half of O_lat's
+// columns); warp 14 forwards receive-buffer releases to the peer (CTA pair
+// only).  Warp w reads TMEM lanes 32*(w%4)..+31.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -50,7 +53,7 @@ constexpr int kKeys = 64;            // keys per tile (S MMA N, O MMA K)
 constexpr int kStages = 4;           // latent tile ring
 constexpr int kXBuf = 4;             // receive buffers of partial S (CTA pair)
 constexpr int kMaxRC = 256;          // rank columns per CTA
-constexpr int kThreads = 480;          // 15 warps
+constexpr int kThreads = 512;          // 16 warps
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
 
 constexpr int kLStage = kKeys * kMaxRC * 2;       // 32 KB
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->x_empty[i], 1);     // forwarded by the peer's forwarding warp
       mbar_init(&bars->x_consumed[i], 8);  // one arrival per local softmax warp
     }
-    mbar_init(&bars->o_last, 1);
+    mbar_init(&bars->o_last, 2);          // one commit per MMA issuer
     mbar_init(&bars->pro_full, 1);
     mbar_init(&bars->pro_done, 1);
     mbar_init(&bars->epi_a, 256);
@@ -273,14 +276,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bars->q_full, 0, 12, nullptr);
       }
     }
-  } else if (warp == 1) {
-    // ======================= MMA issuer =======================
-    // Descriptors are built once per tile and advanced by constants; the issue
-    // sequence is fully unrolled (a single thread issuing tcgen05.mma is the
-    // rate limit for the narrow S MMAs otherwise).  Per tile j, the four long
-    // O(j) += P(j) L(j) MMAs (N = RC) are interleaved with the narrow
-    // S(j+2) = q' L(j+2)^T MMAs (N = 64), so the tensor core always has queued
-    // work while the next instruction is issued.
+  } else if (warp == 1 || warp == 15) {
+    // ======================= MMA issuers =======================
+    // Two issuing threads, lane 0 of warps 1 and 15 (different SM
+    // sub-partitions), take alternate tiles: issuer p owns S buffer p, P buffer
+    // p and tiles j = p (mod 2).  A thread that has just issued MMAs waits for
+    // the tensor core to take them before its next barrier test completes;
+    // with two issuers the other one keeps the tensor core fed meanwhile.
+    // O_lat was zeroed by the softmax warps, so every P.L accumulates and the
+    // order in which the two issuers' O MMAs reach the tensor core is free.
+    // Per tile j, the four long O(j) += P(j) L(j) MMAs (N = RC) are interleaved
+    // with the narrow S(j+2) = q' L(j+2)^T MMAs (N = 64) of the same issuer,
+    // fully unrolled with descriptors advanced by constants.
+    const int par = warp == 1 ? 0 : 1;
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
       constexpr uint32_t idesc_o = make_idesc_bf16(kRows, kRC, false, true);
@@ -290,19 +298,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tq = tmem + kTmemQ;
       bool ok = true;
       if constexpr (kFused) {
-        // q' (fp32, this CTA's rank columns) = q . w_up_k[:, h, c0:c0+RC]^T into O's columns
-        ok = mbar_wait(&bars->pro_full, 0, 24, abort_flag);
-        tc_fence_after();
-        if (ok) {
-          constexpr uint32_t idesc_q = make_idesc_bf16(kRows, kRC, false, false);
-          const uint64_t aq = make_sdesc_sw128(l0, 16, 1024);
-          const uint64_t bw = make_sdesc_sw128(l0 + kFusedWkOff, 16, 1024);
-          for (int k = 0; k < a.d / 16; ++k)
-            umma_bf16(tmem + kTmemO, aq + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
-                      bw + (uint64_t)(((k >> 2) * (kRC * 128) + (k & 3) * 32) >> 4), idesc_q,
-                      k > 0 ? 1u : 0u);
+        if (par == 0) {
+          // q' (fp32, this CTA's rank columns) = q . w_up_k[:, h, c0:c0+RC]^T into O's columns
+          ok = mbar_wait(&bars->pro_full, 0, 24, abort_flag);
+          tc_fence_after();
+          if (ok) {
+            constexpr uint32_t idesc_q = make_idesc_bf16(kRows, kRC, false, false);
+            const uint64_t aq = make_sdesc_sw128(l0, 16, 1024);
+            const uint64_t bw = make_sdesc_sw128(l0 + kFusedWkOff, 16, 1024);
+            for (int k = 0; k < a.d / 16; ++k)
+              umma_bf16(tmem + kTmemO,
+                        aq + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
+                        bw + (uint64_t)(((k >> 2) * (kRC * 128) + (k & 3) * 32) >> 4), idesc_q,
+                        k > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars->pro_done);
         }
-        umma_commit(&bars->pro_done);
       }
       ok = ok && mbar_wait(&bars->q_ready, 0, 20, abort_flag);
       tc_fence_after();
@@ -311,18 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   umma_bf16_ta((sbuf), tq + (k) * 8,                                                     \
                (bd) + (uint64_t)((((k) >> 2) * (kKeys * 128) + ((k) & 3) * 32) >> 4), idesc_s, \
                (k) > 0 ? 1u : 0u)
-      // Small scheduler: S(js) as soon as latent tile js has landed and the
-      // readers of S(js-2) have let its buffer go; O(jo) as soon as P(jo) is
-      // written.  When both are ready, the narrow S K-steps are interleaved
-      // with the long O K-steps so the tensor core always has queued work.
-      int js = 0, jo = 0;
+      // Small scheduler over this issuer's tiles: S(js) as soon as latent tile
+      // js has landed and the readers of S(js-2) have let its buffer go; O(jo)
+      // as soon as P(jo) is written.  When both are ready, the narrow S K-steps
+      // are interleaved with the long O K-steps.
+      int js = par, jo = par;
+      const uint32_t sbuf = tmem + kTmemS + par * kKeys;
+      const uint32_t pbuf = p0 + par * kPBytes;
       const unsigned long long t_start = globaltimer_ns();
       unsigned spins = 0;
       while (ok && jo < nt) {
         const bool s_ready =
             js < nt && mbar_test(smem_u32(&bars->l_full[js % kStages]), (js / kStages) & 1) &&
-            mbar_test(smem_u32(&bars->s_empty[js & 1]), ((js >> 1) & 1) ^ 1);
-        const bool o_ready = jo < js && mbar_test(smem_u32(&bars->p_full[jo & 1]), (jo >> 1) & 1);
+            mbar_test(smem_u32(&bars->s_empty[par]), ((js >> 1) & 1) ^ 1);
+        const bool o_ready = jo < js && mbar_test(smem_u32(&bars->p_full[par]), (jo >> 1) & 1);
         if (!s_ready && !o_ready) {
           // back off: this warp shares an SM sub-partition with softmax warps
           __nanosleep(32);
@@ -336,51 +349,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         uint64_t bds = 0;
-        uint32_t sbuf = 0;
-        if (s_ready) {
-          bds = make_sdesc_sw128(l0 + (js % kStages) * kLStage, 16, 1024);
-          sbuf = tmem + kTmemS + (js & 1) * kKeys;
-        }
+        if (s_ready) bds = make_sdesc_sw128(l0 + (js % kStages) * kLStage, 16, 1024);
         if (o_ready) {
-          const uint64_t ad = make_sdesc_sw128(p0 + (jo & 1) * kPBytes, 16, 1024);
+          const uint64_t ad = make_sdesc_sw128(pbuf, 16, 1024);
           const uint64_t bdo = make_sdesc_sw128(l0 + (jo % kStages) * kLStage, kKeys * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
             umma_bf16(tmem + kTmemO, ad + (uint64_t)((kk * 32) >> 4),
-                      bdo + (uint64_t)((kk * 2048) >> 4), idesc_o, (jo > 0 || kk > 0) ? 1u : 0u);
+                      bdo + (uint64_t)((kk * 2048) >> 4), idesc_o, 1u);
             if (s_ready) {
 #pragma unroll
               for (int q = 0; q < kSPerO; ++q) MLA_S_STEP(sbuf, bds, kk * kSPerO + q);
             }
           }
-          umma_commit(&bars->p_empty[jo & 1]);
+          umma_commit(&bars->p_empty[par]);
           umma_commit(&bars->l_empty[jo % kStages]);
-          ++jo;
+          jo += 2;
         } else {
 #pragma unroll
           for (int k = 0; k < kSSteps; ++k) MLA_S_STEP(sbuf, bds, k);
         }
         if (s_ready) {
-          umma_commit(&bars->s_full[js & 1]);
-          ++js;
+          umma_commit(&bars->s_full[par]);
+          js += 2;
         }
       }
 #undef MLA_S_STEP
       umma_commit(&bars->o_last);
       if constexpr (kFused) {
-        // out_partial = O_lat(bf16, smem) . w_up_v[c0:c0+RC, h, :] into S's columns
-        if (ok && mbar_wait(&bars->epi_a, 0, 25, abort_flag) &&
-            mbar_wait(&bars->epi_w, 0, 26, abort_flag)) {
-          tc_fence_after();
-          const uint32_t idesc_v = make_idesc_bf16(kRows, a.d, false, true);
-          const uint64_t ao = make_sdesc_sw128(l0, 16, 1024);
-          const uint64_t bv = make_sdesc_sw128(l0 + kFusedWvOff, kRC * 128, 1024);
+        if (par == 0) {
+          // out_partial = O_lat(bf16, smem) . w_up_v[c0:c0+RC, h, :] into S's columns
+          if (ok && mbar_wait(&bars->epi_a, 0, 25, abort_flag) &&
+              mbar_wait(&bars->epi_w, 0, 26, abort_flag)) {
+            tc_fence_after();
+            const uint32_t idesc_v = make_idesc_bf16(kRows, a.d, false, true);
+            const uint64_t ao = make_sdesc_sw128(l0, 16, 1024);
+            const uint64_t bv = make_sdesc_sw128(l0 + kFusedWvOff, kRC * 128, 1024);
 #pragma unroll
-          for (int k = 0; k < kRC / 16; ++k)
-            umma_bf16(tmem + kTmemS, ao + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
-                      bv + (uint64_t)((k * 2048) >> 4), idesc_v, k > 0 ? 1u : 0u);
+            for (int k = 0; k < kRC / 16; ++k)
+              umma_bf16(tmem + kTmemS,
+                        ao + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
+                        bv + (uint64_t)((k * 2048) >> 4), idesc_v, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars->epi_done);
         }
-        umma_commit(&bars->epi_done);
       }
     }
   } else if (warp < 6) {
@@ -514,6 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       }
       if (ok) {
+        // O_lat starts at zero (every P.L accumulates): my quadrant, my half of the columns
+        float z[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[e] = 0.f;
+        for (int c = oc0; c < oc0 + RC / 2; c += 32) tmem_st32(tmem + lane_base + kTmemO + c, z);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->q_ready);
@@ -589,7 +606,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_half = l_half * alpha + tree_sum32(s);
       m_run = m_ref;
 
-      // rescale my half of O_lat's columns (only after the previous P.L has landed)
+      // P(j-2).L(j-2) has finished reading P buffer bi
+      if (!warp_wait(&bars->p_empty[bi], (k & 1) ^ 1, 34, abort_flag)) { ok = false; break; }
+      // rescale my half of O_lat's columns once every earlier P.L has landed:
+      // O(j-1) and O(j-2) complete (each issuer's commit covers its earlier MMAs)
       if (__any_sync(0xffffffffu, grow_max && j > 0)) {
         if (!warp_wait(&bars->p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, 33, abort_flag)) {
           ok = false;
@@ -608,7 +628,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // P (bf16) into the K-major swizzled P buffer: my 4 of the row's 8 chunks
-      if (!warp_wait(&bars->p_empty[bi], (k & 1) ^ 1, 34, abort_flag)) { ok = false; break; }
       const uint32_t pb = smem_u32(sP + bi * kPBytes);
 #pragma unroll
       for (int c = 0; c < 4; ++c)
