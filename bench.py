@@ -262,28 +262,61 @@ def run_ours(args, rank: int, world: int):
     ms_per_step = total_ms / args.steps
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
 
-    # --- end to end: pinned host inputs -> device -> path -> host result
+    # --- end to end: pinned host inputs -> device -> path -> host result.
+    # Every step copies its inputs from pinned host memory and its result back.
+    # The copies run on their own streams into / out of double-buffered device
+    # tensors, so step k's compute overlaps the input copy of step k+1 and the
+    # result copy of step k-1 (host<->device copies in both directions and the
+    # kernels run concurrently); the timed region spans the first input copy to
+    # the last result copy.
     host = {k: v.pin_memory() for k, v in x.items() if k != "kv_latent"}
-    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    host_out = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
     e2e_steps = max(3, min(args.steps, 10))
+    dbuf = [d, {k_: torch.empty_like(v_) for k_, v_ in d.items()}]
+    obuf = [out, torch.empty_like(out)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step():
-        for k_, v_ in host.items():
-            d[k_].copy_(v_, non_blocking=True)
-        step()
-        host_out.copy_(out, non_blocking=True)
+    def ev():
+        return torch.cuda.Event()
 
-    e2e_step()
-    torch.cuda.synchronize()
-    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    es.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    ee.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = es.elapsed_time(ee)
+    def e2e_run(n):
+        in_ready = [ev(), ev()]
+        in_free = [None, None]          # compute done with input buffer i
+        computed = [ev(), ev()]
+        out_free = [None, None]         # result copy of output buffer i done
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        for k_ in range(n):
+            i = k_ & 1
+            with torch.cuda.stream(s_in):
+                if in_free[i] is not None:
+                    s_in.wait_event(in_free[i])
+                for name, hv in host.items():
+                    dbuf[i][name].copy_(hv, non_blocking=True)
+                in_ready[i].record(s_in)
+            stream.wait_event(in_ready[i])
+            if out_free[i] is not None:
+                stream.wait_event(out_free[i])
+            mla.project(dbuf[i]["hidden"], dbuf[i]["w_down"], latent=lat)
+            mla.attention(dbuf[i]["q"], lat, dbuf[i]["w_up_k"], dbuf[i]["w_up_v"], w.scale, True,
+                          out=obuf[i], workspace=ws)
+            computed[i].record(stream)
+            in_free[i] = ev()
+            in_free[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[i])
+                host_out[i].copy_(obuf[i], non_blocking=True)
+                out_free[i] = ev()
+                out_free[i].record(s_out)
+        t1.record(s_out)                # the last result copy is the last operation
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    e2e_run(2)
+    e2e_ms = e2e_run(e2e_steps)
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -360,7 +393,9 @@ def run_ours(args, rank: int, world: int):
                      "flops_per_launch": flops_flash, "traffic": flash_traffic(),
                      "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "overlap": "input copy of step k+1 and result copy of step k-1 run on their own "
+                           "streams during step k (double-buffered device tensors)"},
         "gpu_launches": int(launches),
         "clocks": clocks,
         "decode": dec,
