@@ -365,6 +365,49 @@ def run_ours(args, rank: int, world: int):
                "flash_frac_hbm": round(268435456 * 1.0 / (dflash * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                        4)}
 
+    # --- comparator: the same prefill step with k and v materialised (projection
+    # with w_up_k / w_up_v outputs, then attention over explicit k, v)
+    expl = None
+    if not args.no_explicit:
+        kb = torch.empty(w.B, w.Tkv, w.H * w.d, device=dev, dtype=torch.bfloat16)
+        vb = torch.empty_like(kb)
+        shp = (w.B, w.Tkv, w.H, w.d)
+
+        def xstep():
+            lat_, k_, v_ = mla.project(d["hidden"], d["w_down"], d["w_up_k"], d["w_up_v"],
+                                       latent=lat)
+            mla.explicit_attention(d["q"], k_.reshape(shp), v_.reshape(shp), w.scale, True,
+                                   out=out)
+
+        for _ in range(max(3, args.warmup)):
+            xstep()
+        n = max(5, min(args.steps, 20))
+        xev = [mla.StageEvents() for _ in range(n)]
+        xs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        xe = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        torch.cuda.synchronize()
+        for k_i in range(n):
+            flush.zero_()
+            xev[k_i].install()
+            xs[k_i].record(stream)
+            xstep()
+            xe[k_i].record(stream)
+        torch.cuda.synchronize()
+        mla.StageEvents.uninstall()
+        xms = statistics.mean(a.elapsed_time(b) for a, b in zip(xs, xe))
+        xattn = statistics.mean(e.elapsed_ms(1) for e in xev)
+        xflops_attn = 4 * w.d * w.pairs() * w.H            # q.k and p.v over d
+        expl = {"workload": "prefill_bf16, k and v materialised (bf16) by the projection, then "
+                            "attention over explicit k, v",
+                "ms_per_step": round(xms, 4),
+                "attention_ms": round(xattn, 4),
+                "projection_with_kv_ms": round(xms - xattn, 4),
+                "TFLOP_per_s_absorbed_count": round(flops_step / (xms * 1e-3) / 1e12, 2),
+                "attention_TFLOP_per_s_explicit_count": round(xflops_attn / (xattn * 1e-3) / 1e12,
+                                                              2),
+                "attention_frac_explicit_count": round(
+                    xflops_attn / (xattn * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+
     if rank != 0:
         return
     flash_avg = statistics.mean(flash_ms)
@@ -399,6 +442,7 @@ def run_ours(args, rank: int, world: int):
         "gpu_launches": int(launches),
         "clocks": clocks,
         "decode": dec,
+        "explicit_kv_comparator": expl,
     }
     if cpu_val is not None:
         line["cpu_baseline"] = {**cpu_detail, "value": round(cpu_val, 6), "unit": "TFLOP/s"}
@@ -413,6 +457,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-explicit", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -168,6 +168,29 @@ mla_status_t mla_latent_attention_noalloc(const void* q, const void* kv_latent,
                                           void* stream);
 
 /*
+ * Attention over materialised keys and values: the formulation of page
+ * "FW-GLM-5-1 l2_p31" ("The algorithm") with k_s = latent_s @ w_up_k[:,h] and
+ * v_s = latent_s @ w_up_v[:,h] computed beforehand (mla_kv_latent_project with
+ * k and v outputs) instead of absorbed:
+ *   out[b,i,h,:] = sum_{s <= t} softmax_s(scale * q[b,i,h] . k[b,s,h]) v[b,s,h,:],
+ *   t = (Tkv - Tq) + i; causal = 0 -> all s < Tkv.
+ * It computes the same attention as mla_latent_attention with 4*d instead of
+ * 4*rank multiply-adds per (query, key) pair, at the price of writing and
+ * reading k and v (2 * B*Tkv*H*d values).  It serves as the comparator for
+ * the absorbed path.
+ *   q    (B, Tq, H, d)  bf16, row-major
+ *   k, v (B, Tkv, H, d) bf16, row-major
+ *   out  (B, Tq, H, d)  out_dtype (MLA_F32 or MLA_BF16), written
+ * d must be 64 or 128; in_dtype must be MLA_BF16; every pointer 16-byte
+ * aligned (MLA_ERR_SHAPE / MLA_ERR_DTYPE / MLA_ERR_ALIGN otherwise).  One
+ * tensor-core kernel (fp32 accumulation, P rounded to bf16 as in the absorbed
+ * path), no workspace, asynchronous on stream.
+ */
+mla_status_t mla_explicit_attention(const void* q, const void* k, const void* v, void* out, int B,
+                                    int Tq, int Tkv, int H, int d, float scale, int causal,
+                                    int in_dtype, int out_dtype, void* stream);
+
+/*
  * Split-KV merge (the online-softmax merge of partial states; page
  * "Kimi-K2.6 l2_p29", online softmax with running max and rescaling by
  * exp(m - m_new), -inf handling): for each row r and part p < parts,

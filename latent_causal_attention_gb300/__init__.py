@@ -18,7 +18,8 @@ import torch
 from . import _lib
 from ._lib import MLAError, MLA_BF16, MLA_F32
 
-__all__ = ["project", "attention", "attention_from_host", "workspace_size", "merge_partials",
+__all__ = ["project", "attention", "explicit_attention", "attention_from_host", "workspace_size",
+           "merge_partials",
            "set_option", "device_error", "launch_count", "StageEvents", "MLAError",
            "dtype_code"]
 
@@ -104,6 +105,25 @@ def attention(q: torch.Tensor, kv_latent: torch.Tensor, w_up_k: torch.Tensor,
                                   dtype_code(q.dtype), dtype_code(out.dtype), _ptr(workspace),
                                   0 if workspace is None else workspace.numel(), _stream(dev))
     _lib.check("mla_latent_attention", st)
+    return out
+
+
+def explicit_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
+                       causal: bool = True, *, out_dtype: torch.dtype = torch.float32,
+                       out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Attention over materialised keys and values (the comparator of the
+    absorbed path): q (B,Tq,H,d), k / v (B,Tkv,H,d), all bf16, d 64 or 128;
+    returns out (B,Tq,H,d) in ``out_dtype``.  k and v come from ``project``
+    with w_up_k / w_up_v."""
+    lib = _lib.load()
+    B, Tq, H, d = q.shape
+    Tkv = k.shape[1]
+    if out is None:
+        out = torch.empty(B, Tq, H, d, device=q.device, dtype=out_dtype)
+    st = lib.mla_explicit_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Tq, Tkv, H, d,
+                                    float(scale), int(causal), dtype_code(q.dtype),
+                                    dtype_code(out.dtype), _stream(q.device))
+    _lib.check("mla_explicit_attention", st)
     return out
 
 

@@ -124,6 +124,12 @@ __device__ __forceinline__ uint32_t xrow_offset(uint32_t r, uint32_t ch, uint32_
   return r * row_bytes + (((ch & ~7u) | ((ch ^ r) & 7u)) << 4);
 }
 
+// Two bf16 values (low half first) times s, rounded back to bf16 (bf16 -> fp32
+// is exact: the bf16 bits are the high half of the fp32 word).
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t u, float s) {
+  return pack_bf16x2(__uint_as_float(u << 16) * s, __uint_as_float(u & 0xffff0000u) * s);
+}
+
 // Pairwise (tree) max / sum of 32 values: log-depth dependency chains.
 __device__ __forceinline__ float tree_max32(const float (&v)[32]) {
   float a[16];
@@ -147,7 +153,12 @@ __device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
   return (a[0] + a[2]) + (a[1] + a[3]);
 }
 
-template <int kRC, bool kFused>
+// Kernel modes: head-packed rows with q' from the workspace; the fused per-head
+// prefill (absorption and w_up_v inside); explicit K/V (per-head rows, K and V
+// tiles in place of the latent, no up-projections).
+constexpr int kModePacked = 0, kModeFused = 1, kModeExplicit = 2;
+
+template <int kRC, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_packed_kernel(const __grid_constant__ CUtensorMap mapQ,
                         const __grid_constant__ CUtensorMap mapL,
@@ -162,6 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort_flag = &bars->abort_flag;
 
+  constexpr bool kFused = kMode == kModeFused;
+  constexpr bool kExplicit = kMode == kModeExplicit;
+  constexpr bool kPerHead = kMode != kModePacked;     // rows = query positions of one head
+  static_assert(!kExplicit || kRC <= 128, "K and V tiles share one 32 KB stage");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int csize = a.pair ? 2 : 1;
   const uint32_t crank = a.pair ? cluster_ctarank() : 0u;
@@ -171,15 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Head-packed rows: row = i*H + h of one batch entry (q' from the workspace).
   // Fused prefill rows: row = query position i of one (batch entry, head).
   const int work = blockIdx.x / csize;
-  const int per_rb = kFused ? a.B * a.H : a.B * a.splits;
+  const int per_rb = kPerHead ? a.B * a.H : a.B * a.splits;
   const int rb = a.row_blocks - 1 - work / per_rb;
-  const int b = kFused ? (work % per_rb) / a.H : (work / a.splits) % a.B;
-  const int head = kFused ? work % a.H : 0;
-  const int sp = kFused ? 0 : work % a.splits;
-  const int rows_b = kFused ? a.Tq : a.Tq * a.H;
+  const int b = kPerHead ? (work % per_rb) / a.H : (work / a.splits) % a.B;
+  const int head = kPerHead ? work % a.H : 0;
+  const int sp = kPerHead ? 0 : work % a.splits;
+  const int rows_b = kPerHead ? a.Tq : a.Tq * a.H;
   const int row0 = rb * kRows;
   const int last_row = min(row0 + kRows, rows_b) - 1;
-  const int t_max = a.Tkv - a.Tq + (kFused ? last_row : last_row / a.H);
+  const int t_max = a.Tkv - a.Tq + (kPerHead ? last_row : last_row / a.H);
   const int kv_len = a.causal ? min(t_max + 1, a.Tkv) : a.Tkv;
   const int n_tiles_all = (kv_len + kKeys - 1) / kKeys;
   const int per_split = (n_tiles_all + a.splits - 1) / a.splits;
@@ -188,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int RC = kRC;                  // rank columns per CTA
   const int c0 = (int)crank * RC;          // first rank column of this CTA
   constexpr int nchunk = RC / 64;
+  constexpr uint32_t kVOff = kKeys * kRC * 2;   // explicit mode: V tile after the K tile
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -241,6 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       c0);
         }
         mbar_wait(&bars->pro_done, 0, 13, abort_flag);
+      } else if constexpr (kExplicit) {
+        // q tile (128 positions x d of one head) into the staging area
+        mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
+        for (int kc = 0; kc < nchunk; ++kc)
+          tma_load_3d(sP + kc * (kRows * 128), &mapQ, &bars->q_full, 64 * kc, head,
+                      b * a.Tq + row0);
       } else {
         mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
         for (int kc = 0; kc < nchunk; ++kc)
@@ -250,11 +272,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nt; ++j) {
         const int st = j % kStages;
         if (!mbar_wait(&bars->l_empty[st], ((j / kStages) & 1) ^ 1, 10, abort_flag)) break;
-        mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(kKeys * RC * 2));
         uint8_t* dst = sL + st * kLStage;
-        for (int kc = 0; kc < nchunk; ++kc)
-          tma_load_3d(dst + kc * (kKeys * 128), &mapL, &bars->l_full[st], c0 + 64 * kc,
-                      (tile0 + j) * kKeys, b);
+        if constexpr (kExplicit) {
+          // K and V tiles (64 keys x d of one head); keys past this sequence's end
+          // belong to the next one (or are zero-filled) and are masked
+          mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(2 * kKeys * RC * 2));
+          const int key = b * a.Tkv + (tile0 + j) * kKeys;
+          for (int kc = 0; kc < nchunk; ++kc) {
+            tma_load_3d(dst + kc * (kKeys * 128), &mapL, &bars->l_full[st], 64 * kc, head, key);
+            tma_load_3d(dst + kVOff + kc * (kKeys * 128), &mapWk, &bars->l_full[st], 64 * kc,
+                        head, key);
+          }
+        } else {
+          mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(kKeys * RC * 2));
+          for (int kc = 0; kc < nchunk; ++kc)
+            tma_load_3d(dst + kc * (kKeys * 128), &mapL, &bars->l_full[st], c0 + 64 * kc,
+                        (tile0 + j) * kKeys, b);
+        }
         ++issued;
       }
       // Do not leave copies in flight: wait for the last loads of each stage.
@@ -352,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s_ready) bds = make_sdesc_sw128(l0 + (js % kStages) * kLStage, 16, 1024);
         if (o_ready) {
           const uint64_t ad = make_sdesc_sw128(pbuf, 16, 1024);
-          const uint64_t bdo = make_sdesc_sw128(l0 + (jo % kStages) * kLStage, kKeys * 128, 1024);
+          const uint64_t bdo = make_sdesc_sw128(
+              l0 + (jo % kStages) * kLStage + (kExplicit ? kVOff : 0u), kKeys * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
             umma_bf16(tmem + kTmemO, ad + (uint64_t)((kk * 32) >> 4),
@@ -475,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = qd * 32 + lane;                 // row within the tile
     const int grow = row0 + r;                    // row within batch entry b
     const bool row_valid = grow < rows_b;
-    const int t_row = a.Tkv - a.Tq + (row_valid ? (kFused ? grow : grow / a.H) : 0);
+    const int t_row = a.Tkv - a.Tq + (row_valid ? (kPerHead ? grow : grow / a.H) : 0);
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const uint32_t x_local = smem_u32(sX);
     float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2][128] partner exchange
@@ -517,6 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : "=r"(u0), "=r"(u1), "=r"(u2), "=r"(u3)
                          : "r"(addr)
                          : "memory");
+            if constexpr (kExplicit) {     // raw q: fold in scale * log2(e)
+              u0 = scale_bf16x2(u0, a.qscale); u1 = scale_bf16x2(u1, a.qscale);
+              u2 = scale_bf16x2(u2, a.qscale); u3 = scale_bf16x2(u3, a.qscale);
+            }
             asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
                              tmem + lane_base + kTmemQ + kc * 32 + c * 4),
                          "r"(u0), "r"(u1), "r"(u2), "r"(u3)
@@ -724,6 +763,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    } else if constexpr (kExplicit) {
+      // out[b, i, h, :] = O / l, fp32 or bf16; my half of the d columns
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      const int64_t orow = (((int64_t)b * a.Tq + grow) * a.H + head) * a.d;
+      for (int c = oc0; c < oc0 + RC / 2; c += 32) {
+        float o[32];
+        if (have_o) {
+          tmem_ld32(tmem + lane_base + kTmemO + c, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (!row_valid) continue;
+        if (a.out_bf16) {
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                               pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                               pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                               pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+        } else {
+          float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d4[q] = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv,
+                                o[4 * q + 3] * inv);
+        }
+      }
     } else {
       if (a.splits == 1) {
         const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -850,16 +919,16 @@ cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, cudaStream_t 
   return cudaGetLastError();
 }
 
-template <int kRC, bool kFused>
+template <int kRC, int kMode>
 static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                   const CUtensorMap& mapWk, const CUtensorMap& mapWv,
                                   const FlashArgs& args, cudaStream_t stream) {
-  auto kern = flash_packed_kernel<kRC, kFused>;
+  auto kern = flash_packed_kernel<kRC, kMode>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int csize = args.pair ? 2 : 1;
-  const int per_rb = kFused ? args.B * args.H : args.B * args.splits;
+  const int per_rb = kMode != kModePacked ? args.B * args.H : args.B * args.splits;
   const unsigned blocks = (unsigned)(args.row_blocks * per_rb * csize);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks, 1, 1);
@@ -881,10 +950,10 @@ static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& m
 cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                 const FlashArgs& args, cudaStream_t stream) {
   switch (args.RC) {
-    case 64: return launch_flash_rc<64, false>(mapQ, mapL, mapQ, mapQ, args, stream);
-    case 128: return launch_flash_rc<128, false>(mapQ, mapL, mapQ, mapQ, args, stream);
-    case 192: return launch_flash_rc<192, false>(mapQ, mapL, mapQ, mapQ, args, stream);
-    case 256: return launch_flash_rc<256, false>(mapQ, mapL, mapQ, mapQ, args, stream);
+    case 64: return launch_flash_rc<64, kModePacked>(mapQ, mapL, mapQ, mapQ, args, stream);
+    case 128: return launch_flash_rc<128, kModePacked>(mapQ, mapL, mapQ, mapQ, args, stream);
+    case 192: return launch_flash_rc<192, kModePacked>(mapQ, mapL, mapQ, mapQ, args, stream);
+    case 256: return launch_flash_rc<256, kModePacked>(mapQ, mapL, mapQ, mapQ, args, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -893,10 +962,20 @@ cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                const CUtensorMap& mapWk, const CUtensorMap& mapWv,
                                const FlashArgs& args, cudaStream_t stream) {
   switch (args.RC) {
-    case 64: return launch_flash_rc<64, true>(mapQ, mapL, mapWk, mapWv, args, stream);
-    case 128: return launch_flash_rc<128, true>(mapQ, mapL, mapWk, mapWv, args, stream);
-    case 192: return launch_flash_rc<192, true>(mapQ, mapL, mapWk, mapWv, args, stream);
-    case 256: return launch_flash_rc<256, true>(mapQ, mapL, mapWk, mapWv, args, stream);
+    case 64: return launch_flash_rc<64, kModeFused>(mapQ, mapL, mapWk, mapWv, args, stream);
+    case 128: return launch_flash_rc<128, kModeFused>(mapQ, mapL, mapWk, mapWv, args, stream);
+    case 192: return launch_flash_rc<192, kModeFused>(mapQ, mapL, mapWk, mapWv, args, stream);
+    case 256: return launch_flash_rc<256, kModeFused>(mapQ, mapL, mapWk, mapWv, args, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_flash_explicit(const CUtensorMap& mapQ, const CUtensorMap& mapK,
+                                  const CUtensorMap& mapV, const FlashArgs& args,
+                                  cudaStream_t stream) {
+  switch (args.RC) {
+    case 64: return launch_flash_rc<64, kModeExplicit>(mapQ, mapK, mapV, mapV, args, stream);
+    case 128: return launch_flash_rc<128, kModeExplicit>(mapQ, mapK, mapV, mapV, args, stream);
     default: return cudaErrorInvalidValue;
   }
 }

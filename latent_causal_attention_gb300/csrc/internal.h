@@ -63,6 +63,11 @@ cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL
 
 // Fused prefill: q (3-D map {d, H, B*Tq}, box {64,1,128}), latent, w_up_k
 // (K-major, {d, H, R}, box {64,1,RC}), w_up_v (MN-major, {d, H, R}, box {64,1,64}).
+// Explicit K/V attention: mapQ over q {d, H, B*Tq}, mapK / mapV over k, v
+// {d, H, B*Tkv}; args.RC = args.d (64 or 128), no CTA pair.
+cudaError_t launch_flash_explicit(const CUtensorMap& mapQ, const CUtensorMap& mapK,
+                                  const CUtensorMap& mapV, const FlashArgs& args,
+                                  cudaStream_t stream);
 cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                const CUtensorMap& mapWk, const CUtensorMap& mapWv,
                                const FlashArgs& args, cudaStream_t stream);

@@ -410,6 +410,33 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
   return MLA_OK;
 }
 
+mla_status_t mla_explicit_attention(const void* q, const void* k, const void* v, void* out, int B,
+                                    int Tq, int Tkv, int H, int d, float scale, int causal,
+                                    int in_dtype, int out_dtype, void* stream_) {
+  if (!q || !k || !v || !out) return MLA_ERR_NULL;
+  if (B <= 0 || Tq <= 0 || Tkv <= 0 || H <= 0 || Tq > Tkv) return MLA_ERR_SHAPE;
+  if (d != 64 && d != 128) return MLA_ERR_SHAPE;
+  if ((int64_t)B * Tq * H > ((int64_t)1 << 31) || (int64_t)B * Tkv * H > ((int64_t)1 << 31))
+    return MLA_ERR_SHAPE;
+  if (in_dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (!(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out))) return MLA_ERR_ALIGN;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const uint64_t BT = (uint64_t)B * Tq, BS = (uint64_t)B * Tkv;
+  CUtensorMap mQ, mK, mV;
+  if (!make_tmap_3d(&mQ, q, 2, d, H, BT, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 128, true) ||
+      !make_tmap_3d(&mK, k, 2, d, H, BS, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 64, true) ||
+      !make_tmap_3d(&mV, v, 2, d, H, BS, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 64, true))
+    return MLA_ERR_CUDA;
+  FlashArgs fa = {};
+  fa.B = B; fa.Tq = Tq; fa.Tkv = Tkv; fa.H = H; fa.R = d; fa.RC = d; fa.pair = 0;
+  fa.row_blocks = (Tq + 127) / 128; fa.splits = 1; fa.causal = causal ? 1 : 0;
+  fa.d = d; fa.qscale = scale * 1.4426950408889634f; fa.out = out;
+  fa.out_bf16 = out_dtype == MLA_BF16;
+  return cuda_status(
+      staged(1, stream, [&] { return launch_flash_explicit(mQ, mK, mV, fa, stream); }));
+}
+
 mla_status_t mla_merge_partials(const float* m, const float* l, const float* o, void* out,
                                 int parts, int rows, int width, int out_dtype, void* stream_) {
   if (!m || !l || !o || !out) return MLA_ERR_NULL;

@@ -151,3 +151,18 @@ def make_inputs(w: Workload, seed: Optional[int] = None, *, with_latent: bool = 
     if with_latent:
         out["kv_latent"] = draw((w.B, w.Tkv, w.rank), w.std_latent)
     return out
+
+
+def make_kv_inputs(w: Workload, seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """Queries, keys and values drawn directly (for attention over given k, v):
+    q (B,Tq,H,d), k and v (B,Tkv,H,d), N(0, 1) each (the spread of latent @
+    w_up with the workloads' weight scaling), in the workload's dtype.  Same
+    generator recipe as make_inputs; drawn in the order q, k, v."""
+    g = torch.Generator("cpu").manual_seed(4321 + w.index if seed is None else seed)
+    dt = w.torch_dtype
+
+    def draw(shape):
+        return torch.randn(shape, generator=g, dtype=torch.float32).to(dt).contiguous()
+
+    return {"q": draw((w.B, w.Tq, w.H, w.d)), "k": draw((w.B, w.Tkv, w.H, w.d)),
+            "v": draw((w.B, w.Tkv, w.H, w.d))}

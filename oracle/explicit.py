@@ -38,6 +38,27 @@ def softmax_rows(x: np.ndarray) -> np.ndarray:
     return w / w.sum(axis=-1, keepdims=True)
 
 
+def attention_kv(q, k, v, scale: float, causal: bool = True, query_rows=None) -> np.ndarray:
+    """Ordinary softmax attention over given keys and values: q (B,Tq,H,d),
+    k, v (B,Tkv,H,d) -> out (B,Tq,H,d) float64 (or (B,len(query_rows),H,d)).
+    The same definition with k_s and v_s supplied instead of rebuilt from the
+    latent; queries are the last Tq positions, mask s <= t when causal."""
+    qf, K, V = _f64(q), _f64(k), _f64(v)
+    B, Tq, H, d = qf.shape
+    Tkv = K.shape[1]
+    idx = np.arange(Tq) if query_rows is None else np.asarray(query_rows)
+    t = (Tkv - Tq) + idx
+    out = np.empty((B, len(idx), H, d))
+    s = np.arange(Tkv)
+    for b in range(B):
+        for h in range(H):
+            x = (qf[b, idx, h, :] @ K[b, :, h, :].T) * scale
+            if causal:
+                x = np.where(s[None, :] <= t[:, None], x, -np.inf)
+            out[b, :, h, :] = softmax_rows(x) @ V[b, :, h, :]
+    return out
+
+
 def attention(q, kv_latent, w_up_k, w_up_v, scale: float, causal: bool = True,
               query_rows=None) -> np.ndarray:
     """out (B, Tq, H, d) float64; ``query_rows`` restricts to a subset of i

@@ -72,6 +72,23 @@ def test_attention_validation(lib):
     assert attn(lib, ws=ctypes.c_void_p(16), wsb=need) == 4     # workspace not 256-aligned
 
 
+def test_explicit_attention_validation(lib):
+    """Host-side checks of mla_explicit_attention (no launch reaches a GPU)."""
+    P = ctypes.c_void_p(256)
+
+    def call(q=P, k=P, v=P, out=P, B=1, Tq=8, Tkv=8, H=2, d=64, ind=1, outd=0):
+        return lib.mla_explicit_attention(q, k, v, out, B, Tq, Tkv, H, d, 0.125, 1, ind, outd,
+                                          None)
+    assert call(k=None) == 1
+    assert call(out=None) == 1
+    assert call(B=0) == 2
+    assert call(Tq=9, Tkv=8) == 2
+    assert call(d=96) == 2                       # d must be 64 or 128
+    assert call(ind=0) == 3                      # bf16 inputs only
+    assert call(outd=5) == 3
+    assert call(v=ctypes.c_void_p(264)) == 4     # not 16-byte aligned
+
+
 def test_workspace_size_rules(lib):
     ws = lib.mla_latent_attention_workspace_size
     assert ws(2, 32, 32, 4, 16, 24, 0, 1) == 0                 # fp32: warp path, no workspace

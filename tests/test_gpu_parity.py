@@ -12,7 +12,8 @@ import torch
 
 import latent_causal_attention_gb300 as mla
 from latent_causal_attention_gb300 import _lib
-from latent_causal_attention_gb300.inputs import WORKLOADS, custom_workload, make_inputs
+from latent_causal_attention_gb300.inputs import (WORKLOADS, custom_workload, make_inputs,
+                                                   make_kv_inputs)
 from oracle import explicit
 
 from _util import assert_bf16_close, assert_f32_close, cuda, sample_rows, to_np
@@ -160,6 +161,8 @@ EDGE = [
     dict(B=2, Tq=33, Tkv=100, H=4, d=64, rank=128, causal=False),      # no mask
     dict(B=3, Tq=1, Tkv=1, H=1, d=64, rank=64, causal=True),           # a single key
     dict(B=1, Tq=64, Tkv=64, H=2, d=192, rank=512, causal=True),       # pair, wide head
+    dict(B=1, Tq=96, Tkv=500, H=2, d=128, rank=512, causal=True),      # pair, chunked, ragged
+    dict(B=1, Tq=100, Tkv=260, H=2, d=64, rank=512, causal=False),     # pair, no mask
 ]
 
 
@@ -252,3 +255,55 @@ def test_bounded_wait_reports_timeout_and_context_survives(oracle):
     assert mla.device_error(clear=True) == 0x17F
     assert mla.device_error() == 0
     test_tiny_f32_full(oracle)                                  # the context is still usable
+
+
+# ----------------------------------------------------- explicit K/V comparator
+EXPLICIT = [
+    dict(B=2, Tq=200, Tkv=200, H=3, d=128, causal=True),     # ragged row block
+    dict(B=1, Tq=70, Tkv=300, H=4, d=64, causal=True),       # chunked prefill
+    dict(B=2, Tq=33, Tkv=100, H=2, d=128, causal=False),     # no mask
+    dict(B=3, Tq=1, Tkv=1, H=1, d=64, causal=True),          # a single key
+    dict(B=2, Tq=1, Tkv=777, H=5, d=128, causal=True),       # one query over a ragged key range
+]
+
+
+@pytest.mark.parametrize("shape", EXPLICIT, ids=lambda s: "x".join(str(v) for v in s.values()))
+def test_explicit_attention_parity(shape):
+    """Attention over given k, v (the comparator kernel) against the float64
+    softmax attention over the same bf16 k, v."""
+    w = custom_workload("explicit", dtype="bf16", rank=64, **shape)
+    x = make_kv_inputs(w, seed=31)
+    q, k, v = (cuda(x[n]) for n in ("q", "k", "v"))
+    out = mla.explicit_attention(q, k, v, w.scale, w.causal)
+    outb = mla.explicit_attention(q, k, v, w.scale, w.causal, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    ref = explicit.attention_kv(x["q"], x["k"], x["v"], w.scale, w.causal)
+    assert_bf16_close(to_np(out), ref, f"explicit {shape}")
+    assert_bf16_close(to_np(outb.float()), ref, f"explicit {shape} bf16 out")
+    assert mla.device_error() == 0
+
+
+def test_explicit_path_chain_matches_latent_oracle(oracle):
+    """hidden -> latent, k, v (projection kernels, bf16) -> explicit attention,
+    against the oracle's float64 projection and literal latent attention: the
+    comparator computes the same attention as the absorbed path."""
+    w = custom_workload("explicit_chain", dtype="bf16", B=2, Tq=160, Tkv=160, H=4, d=128,
+                        rank=128, model_dim=256)
+    x = make_inputs(w, seed=33, with_latent=False)
+    _, k, v = mla.project(cuda(x["hidden"]), cuda(x["w_down"]), cuda(x["w_up_k"]),
+                          cuda(x["w_up_v"]))
+    shp = (w.B, w.Tkv, w.H, w.d)
+    out = mla.explicit_attention(cuda(x["q"]), k.reshape(shp), v.reshape(shp), w.scale, True)
+    rl = np.stack([oracle.project(x["hidden"][b], x["w_down"])[0] for b in range(w.B)])
+    # The explicit path stores the latent, k and v as bf16 (the latent feeds the
+    # up-projection in bf16): the same three roundings in the reference, then
+    # the float64 attention over those k, v.  Against the unrounded literal
+    # attention only the normwise error is held to the bf16 bound.
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).double().numpy()
+    kr, vr = explicit.materialise_kv(bf16(rl), x["w_up_k"], x["w_up_v"])
+    ref = explicit.attention_kv(x["q"], bf16(kr), bf16(vr), w.scale, True)
+    assert_bf16_close(to_np(out), ref, "explicit chain")
+    lit = oracle.attention(x["q"], rl, x["w_up_k"], x["w_up_v"], w.scale, True)
+    g = to_np(out)
+    assert np.linalg.norm(g - lit) <= 2e-2 * np.linalg.norm(lit)

@@ -229,3 +229,31 @@ def test_config_workloads_match_their_descriptions():
     assert abs(t["w_up_k"].std().item() * math.sqrt(24) - 1) < 0.1
     t2 = make_inputs(WORKLOADS["tiny_f32"])
     assert torch.equal(t["q"], t2["q"])                  # seeded
+
+
+# ------------------------------------------------- explicit K/V oracle (numpy)
+def test_explicit_kv_oracle_matches_literal(oracle):
+    """attention_kv over K, V materialised in float64 equals the C oracle's
+    literal form, which rebuilds k_s and v_s for every (b, h, t, s)."""
+    q, lat, wk, wv = _small(21, B=2, Tq=6, Tkv=11, H=3, d=5, R=7)
+    K, V = explicit.materialise_kv(lat, wk, wv)
+    for causal in (True, False):
+        ref = oracle.attention(q, lat, wk, wv, 0.6, causal)
+        np.testing.assert_allclose(explicit.attention_kv(q, K, V, 0.6, causal), ref,
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_explicit_kv_oracle_matches_sdpa():
+    """attention_kv equals torch's float64 scaled-dot-product attention (a
+    library routine) with the queries at the last Tq positions."""
+    rng = np.random.default_rng(22)
+    B, Tq, Tkv, H, d = 2, 5, 9, 2, 4
+    q, k, v = (rng.standard_normal(s) for s in [(B, Tq, H, d), (B, Tkv, H, d), (B, Tkv, H, d)])
+    t = (Tkv - Tq) + np.arange(Tq)
+    mask = torch.from_numpy(np.arange(Tkv)[None, :] <= t[:, None])
+    tq, tk, tv = (torch.from_numpy(a).permute(0, 2, 1, 3) for a in (q, k, v))
+    for causal in (True, False):
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk, tv, attn_mask=mask if causal else None, scale=0.35).permute(0, 2, 1, 3)
+        np.testing.assert_allclose(explicit.attention_kv(q, k, v, 0.35, causal), ref.numpy(),
+                                   rtol=1e-12, atol=1e-12)
