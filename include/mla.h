@@ -168,6 +168,33 @@ mla_status_t mla_latent_attention_noalloc(const void* q, const void* kv_latent,
                                           void* stream);
 
 /*
+ * Variable-length batch: the attention of mla_latent_attention for B
+ * sequences of different lengths packed back to back.  Sequence b owns query
+ * rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) of q and out, and latent rows
+ * [cu_seqlens_kv[b], cu_seqlens_kv[b+1]) of kv_latent; its Tq_b queries are
+ * the last Tq_b of its Tkv_b positions (t = Tkv_b - Tq_b + i), causal as in
+ * mla_latent_attention.
+ *   q, out        (total_q, H, d) bf16 / out_dtype
+ *   kv_latent     (total_kv, rank) bf16
+ *   w_up_k/w_up_v (rank, H, d) bf16
+ *   cu_seqlens_q, cu_seqlens_kv: device int32, B+1 non-decreasing entries,
+ *                 [0] = 0, [B] = total_q / total_kv (4-byte aligned)
+ *   max_seqlen_q  the longest query range (sizes the grid)
+ * Needs d 64 or 128, rank a multiple of 64 up to 256 or of 128 up to 512,
+ * bf16 inputs, 16-byte aligned tensors; no workspace (one fused per-head
+ * kernel; a cluster of two CTAs for rank > 256).  A sequence whose ranges do
+ * not satisfy 0 <= Tq_b <= Tkv_b inside the packed tensors is skipped (its
+ * output rows are not written) and recorded in the device error word
+ * (kernel-side code 0x200 | b) read by mla_get_device_error.
+ */
+mla_status_t mla_latent_attention_varlen(const void* q, const void* kv_latent, const void* w_up_k,
+                                         const void* w_up_v, void* out, const int* cu_seqlens_q,
+                                         const int* cu_seqlens_kv, int B, int max_seqlen_q,
+                                         int total_q, int total_kv, int H, int d, int rank,
+                                         float scale, int causal, int in_dtype, int out_dtype,
+                                         void* stream);
+
+/*
  * Attention over materialised keys and values: the formulation of page
  * "FW-GLM-5-1 l2_p31" ("The algorithm") with k_s = latent_s @ w_up_k[:,h] and
  * v_s = latent_s @ w_up_v[:,h] computed beforehand (mla_kv_latent_project with

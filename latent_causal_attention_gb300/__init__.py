@@ -18,7 +18,8 @@ import torch
 from . import _lib
 from ._lib import MLAError, MLA_BF16, MLA_F32
 
-__all__ = ["project", "attention", "explicit_attention", "attention_from_host", "workspace_size",
+__all__ = ["project", "attention", "attention_varlen", "explicit_attention", "attention_from_host",
+           "workspace_size",
            "merge_partials",
            "set_option", "device_error", "launch_count", "StageEvents", "MLAError",
            "dtype_code"]
@@ -105,6 +106,29 @@ def attention(q: torch.Tensor, kv_latent: torch.Tensor, w_up_k: torch.Tensor,
                                   dtype_code(q.dtype), dtype_code(out.dtype), _ptr(workspace),
                                   0 if workspace is None else workspace.numel(), _stream(dev))
     _lib.check("mla_latent_attention", st)
+    return out
+
+
+def attention_varlen(q: torch.Tensor, kv_latent: torch.Tensor, w_up_k: torch.Tensor,
+                     w_up_v: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_kv: torch.Tensor,
+                     max_seqlen_q: int, scale: float, causal: bool = True, *,
+                     out_dtype: torch.dtype = torch.float32,
+                     out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Variable-length batch: q (total_q,H,d), kv_latent (total_kv,rank) packed
+    back to back, cu_seqlens_q / cu_seqlens_kv (B+1,) int32 on the device;
+    returns out (total_q,H,d)."""
+    lib = _lib.load()
+    total_q, H, d = q.shape
+    total_kv, R = kv_latent.shape
+    B = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty(total_q, H, d, device=q.device, dtype=out_dtype)
+    st = lib.mla_latent_attention_varlen(_ptr(q), _ptr(kv_latent), _ptr(w_up_k), _ptr(w_up_v),
+                                         _ptr(out), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B,
+                                         int(max_seqlen_q), total_q, total_kv, H, d, R,
+                                         float(scale), int(causal), dtype_code(q.dtype),
+                                         dtype_code(out.dtype), _stream(q.device))
+    _lib.check("mla_latent_attention_varlen", st)
     return out
 
 

@@ -26,6 +26,8 @@ SIGNATURES = {
                                   _vp, _sz, _vp]),
     "mla_latent_attention_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
                                           _i, _i, _i, _vp]),
+    "mla_latent_attention_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                         _i, _i, _f, _i, _i, _i, _vp]),
     "mla_explicit_attention": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     "mla_merge_partials": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "mla_get_device_error": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),

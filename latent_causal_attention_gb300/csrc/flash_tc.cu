@@ -191,11 +191,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = kPerHead ? (work % per_rb) / a.H : (work / a.splits) % a.B;
   const int head = kPerHead ? work % a.H : 0;
   const int sp = kPerHead ? 0 : work % a.splits;
-  const int rows_b = kPerHead ? a.Tq : a.Tq * a.H;
+  // batch entry b's query rows start at q0 and its keys at kv0 (of the packed
+  // tensors of a variable-length batch, or b*Tq and b*Tkv otherwise)
+  int q0 = b * a.Tq, kv0 = b * a.Tkv, Tq_b = a.Tq, Tkv_b = a.Tkv;
+  const bool varlen = kPerHead && a.cu_q != nullptr;
+  if (varlen) {
+    q0 = a.cu_q[b];
+    Tq_b = a.cu_q[b + 1] - q0;
+    kv0 = a.cu_kv[b];
+    Tkv_b = a.cu_kv[b + 1] - kv0;
+    if (q0 < 0 || Tq_b < 0 || q0 + Tq_b > a.total_q || kv0 < 0 || Tkv_b < Tq_b ||
+        kv0 + Tkv_b > a.total_kv) {
+      if (threadIdx.x == 0 && head == 0 && rb == a.row_blocks - 1 && crank == 0)
+        report_error(kErrBadLengths | (unsigned)(b & 0xff));
+      Tq_b = 0;                            // no rows: nothing read, nothing written
+      Tkv_b = 0;
+    }
+  }
+  const int rows_b = kPerHead ? Tq_b : a.Tq * a.H;
   const int row0 = rb * kRows;
   const int last_row = min(row0 + kRows, rows_b) - 1;
-  const int t_max = a.Tkv - a.Tq + (kPerHead ? last_row : last_row / a.H);
-  const int kv_len = a.causal ? min(t_max + 1, a.Tkv) : a.Tkv;
+  const int t_max = Tkv_b - Tq_b + (kPerHead ? last_row : last_row / a.H);
+  // (a row block past the end of its sequence, possible in a variable-length
+  // batch, has no work)
+  const int kv_len = row0 >= rows_b ? 0 : a.causal ? min(t_max + 1, Tkv_b) : Tkv_b;
   const int n_tiles_all = (kv_len + kKeys - 1) / kKeys;
   const int per_split = (n_tiles_all + a.splits - 1) / a.splits;
   const int tile0 = sp * per_split;
@@ -252,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars->pro_full, (uint32_t)(kRows * a.d * 2 + RC * a.d * 2));
         for (int kc = 0; kc < dch; ++kc) {
           tma_load_3d(sL + kc * (kRows * 128), &mapQ, &bars->pro_full, 64 * kc, head,
-                      b * a.Tq + row0);
+                      q0 + row0);
           tma_load_3d(sL + kFusedWkOff + kc * (RC * 128), &mapWk, &bars->pro_full, 64 * kc, head,
                       c0);
         }
@@ -262,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
         for (int kc = 0; kc < nchunk; ++kc)
           tma_load_3d(sP + kc * (kRows * 128), &mapQ, &bars->q_full, 64 * kc, head,
-                      b * a.Tq + row0);
+                      q0 + row0);
       } else {
         mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
         for (int kc = 0; kc < nchunk; ++kc)
@@ -277,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // K and V tiles (64 keys x d of one head); keys past this sequence's end
           // belong to the next one (or are zero-filled) and are masked
           mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(2 * kKeys * RC * 2));
-          const int key = b * a.Tkv + (tile0 + j) * kKeys;
+          const int key = kv0 + (tile0 + j) * kKeys;
           for (int kc = 0; kc < nchunk; ++kc) {
             tma_load_3d(dst + kc * (kKeys * 128), &mapL, &bars->l_full[st], 64 * kc, head, key);
             tma_load_3d(dst + kVOff + kc * (kKeys * 128), &mapWk, &bars->l_full[st], 64 * kc,
@@ -287,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(kKeys * RC * 2));
           for (int kc = 0; kc < nchunk; ++kc)
             tma_load_3d(dst + kc * (kKeys * 128), &mapL, &bars->l_full[st], c0 + 64 * kc,
-                        (tile0 + j) * kKeys, b);
+                        (varlen ? kv0 : 0) + (tile0 + j) * kKeys, varlen ? 0 : b);
         }
         ++issued;
       }
@@ -510,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = qd * 32 + lane;                 // row within the tile
     const int grow = row0 + r;                    // row within batch entry b
     const bool row_valid = grow < rows_b;
-    const int t_row = a.Tkv - a.Tq + (row_valid ? (kPerHead ? grow : grow / a.H) : 0);
+    const int t_row = Tkv_b - Tq_b + (row_valid ? (kPerHead ? grow : grow / a.H) : 0);
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const uint32_t x_local = smem_u32(sX);
     float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2][128] partner exchange
@@ -623,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // mask: key s_idx visible iff s_idx < Tkv and (not causal or s_idx <= t)
       const int key0 = (tile0 + j) * kKeys + half * 32;
-      const int lim = a.causal ? min(t_row + 1, a.Tkv) : a.Tkv;   // visible keys < lim
+      const int lim = a.causal ? min(t_row + 1, Tkv_b) : Tkv_b;   // visible keys < lim
       if (!row_valid || key0 + 32 > lim) {
 #pragma unroll
         for (int c = 0; c < 32; ++c)
@@ -724,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cfirst = (a.pair ? (int)crank * dh : 0) + half * (dh / 2);
       bool have_peer = true;
       if (a.pair) have_peer = have_out && warp_wait<true>(&bars->epi_x, 0, 37, abort_flag);
-      const int64_t orow = (((int64_t)b * a.Tq + grow) * a.H + head) * a.d;
+      const int64_t orow = (((int64_t)q0 + grow) * a.H + head) * a.d;
       for (int c = cfirst; c < cfirst + dh / 2; c += 16) {
         float v[16];
         if (have_out) {
@@ -766,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if constexpr (kExplicit) {
       // out[b, i, h, :] = O / l, fp32 or bf16; my half of the d columns
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      const int64_t orow = (((int64_t)b * a.Tq + grow) * a.H + head) * a.d;
+      const int64_t orow = (((int64_t)q0 + grow) * a.H + head) * a.d;
       for (int c = oc0; c < oc0 + RC / 2; c += 32) {
         float o[32];
         if (have_o) {

@@ -57,6 +57,12 @@ struct FlashArgs {
   void* olat;        // splits == 1: normalised latent-space output, bf16 (B*Tq*H, R)
   float* part_o;     // splits > 1: (splits, B*Tq*H, R) unnormalised
   float* part_ml;    // splits > 1: (splits, B*Tq*H, 2) = (max in log2 units, sum)
+  // variable-length batch (per-head modes only): batch entry b owns query rows
+  // [cu_q[b], cu_q[b+1]) of total_q and latent rows [cu_kv[b], cu_kv[b+1]) of
+  // total_kv (device int32, B+1 entries); Tq is then the longest query range.
+  const int* cu_q;
+  const int* cu_kv;
+  int total_q, total_kv;
 };
 cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                 const FlashArgs& args, cudaStream_t stream);

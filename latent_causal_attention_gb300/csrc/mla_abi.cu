@@ -410,6 +410,51 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
   return MLA_OK;
 }
 
+mla_status_t mla_latent_attention_varlen(const void* q, const void* kv_latent, const void* w_up_k,
+                                         const void* w_up_v, void* out, const int* cu_seqlens_q,
+                                         const int* cu_seqlens_kv, int B, int max_seqlen_q,
+                                         int total_q, int total_kv, int H, int d, int rank,
+                                         float scale, int causal, int in_dtype, int out_dtype,
+                                         void* stream_) {
+  if (!q || !kv_latent || !w_up_k || !w_up_v || !out || !cu_seqlens_q || !cu_seqlens_kv)
+    return MLA_ERR_NULL;
+  if (B <= 0 || max_seqlen_q <= 0 || total_q <= 0 || total_kv <= 0 || H <= 0 ||
+      max_seqlen_q > total_q)
+    return MLA_ERR_SHAPE;
+  if ((int64_t)total_q * H > ((int64_t)1 << 31)) return MLA_ERR_SHAPE;
+  if (d % 64 != 0 || d > 128 || !tc_shape_ok(d, rank)) return MLA_ERR_SHAPE;
+  if (in_dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (!(aligned16(q) && aligned16(kv_latent) && aligned16(w_up_k) && aligned16(w_up_v) &&
+        aligned16(out)) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3) != 0 ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_kv) & 3) != 0)
+    return MLA_ERR_ALIGN;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const int R = rank;
+  const int pair = R > 256 ? 1 : 0;
+  const int RC = pair ? R / 2 : R;
+  CUtensorMap mQ, mL, mWk, mWv;
+  if (!make_tmap_3d(&mQ, q, 2, d, H, (uint64_t)total_q, (uint64_t)d * 2, (uint64_t)H * d * 2, 64,
+                    1, 128, true) ||
+      !make_tmap_3d(&mL, kv_latent, 2, R, (uint64_t)total_kv, 1, (uint64_t)R * 2,
+                    (uint64_t)total_kv * R * 2, 64, 64, 1, true) ||
+      !make_tmap_3d(&mWk, w_up_k, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, RC,
+                    true) ||
+      !make_tmap_3d(&mWv, w_up_v, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 64,
+                    true))
+    return MLA_ERR_CUDA;
+  FlashArgs fa = {};
+  fa.B = B; fa.Tq = max_seqlen_q; fa.Tkv = 0; fa.H = H; fa.R = R; fa.RC = RC; fa.pair = pair;
+  fa.row_blocks = (max_seqlen_q + 127) / 128; fa.splits = 1; fa.causal = causal ? 1 : 0;
+  fa.d = d; fa.qscale = scale * 1.4426950408889634f; fa.out = out;
+  fa.out_bf16 = out_dtype == MLA_BF16;
+  fa.cu_q = cu_seqlens_q; fa.cu_kv = cu_seqlens_kv;
+  fa.total_q = total_q; fa.total_kv = total_kv;
+  return cuda_status(
+      staged(1, stream, [&] { return launch_flash_fused(mQ, mL, mWk, mWv, fa, stream); }));
+}
+
 mla_status_t mla_explicit_attention(const void* q, const void* k, const void* v, void* out, int B,
                                     int Tq, int Tkv, int H, int d, float scale, int causal,
                                     int in_dtype, int out_dtype, void* stream_) {

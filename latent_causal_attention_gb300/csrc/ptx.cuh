@@ -22,6 +22,7 @@ static __device__ unsigned int g_device_error = 0;
 enum : unsigned int {
   kErrNone = 0,
   kErrWaitTimeout = 0x100,   // | site id in the low byte
+  kErrBadLengths = 0x200,    // variable-length batch: cumulative lengths out of range
 };
 
 // Upper bound for any single wait on an mbarrier (nanoseconds of globaltimer).

@@ -89,6 +89,23 @@ def test_explicit_attention_validation(lib):
     assert call(v=ctypes.c_void_p(264)) == 4     # not 16-byte aligned
 
 
+def test_varlen_validation(lib):
+    """Host-side checks of mla_latent_attention_varlen (no launch reaches a GPU)."""
+    P = ctypes.c_void_p(256)
+
+    def call(q=P, cu=P, B=2, maxq=8, tq=16, tkv=16, H=2, d=64, R=128, ind=1, outd=0, cuk=P):
+        return lib.mla_latent_attention_varlen(q, P, P, P, P, cu, cuk, B, maxq, tq, tkv, H, d, R,
+                                               0.125, 1, ind, outd, None)
+    assert call(q=None) == 1
+    assert call(cu=None) == 1
+    assert call(B=0) == 2
+    assert call(maxq=17) == 2                    # longer than all queries together
+    assert call(d=192) == 2                      # d 64 or 128
+    assert call(R=96) == 2                       # rank a multiple of 64
+    assert call(ind=0) == 3                      # bf16 inputs only
+    assert call(cuk=ctypes.c_void_p(258)) == 4   # int32 offsets 4-byte aligned
+
+
 def test_workspace_size_rules(lib):
     ws = lib.mla_latent_attention_workspace_size
     assert ws(2, 32, 32, 4, 16, 24, 0, 1) == 0                 # fp32: warp path, no workspace

@@ -307,3 +307,66 @@ def test_explicit_path_chain_matches_latent_oracle(oracle):
     lit = oracle.attention(x["q"], rl, x["w_up_k"], x["w_up_v"], w.scale, True)
     g = to_np(out)
     assert np.linalg.norm(g - lit) <= 2e-2 * np.linalg.norm(lit)
+
+
+# ------------------------------------------------------ variable-length batch
+VARLEN = [
+    dict(lens=[(130, 130), (1, 50), (64, 300), (200, 257)], H=3, d=128, rank=512, causal=True),
+    dict(lens=[(70, 70), (5, 9), (128, 128)], H=2, d=64, rank=256, causal=True),
+    dict(lens=[(33, 100), (129, 140)], H=2, d=128, rank=512, causal=False),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=lambda c: f"R{c['rank']}d{c['d']}n{len(c['lens'])}"
+                         f"{'c' if c['causal'] else 'nc'}")
+def test_varlen_batch_matches_per_sequence_oracle(oracle, case):
+    """Sequences of different lengths packed back to back, one call, against
+    the oracle run on each sequence alone."""
+    H, d, R = case["H"], case["d"], case["rank"]
+    w0 = custom_workload("varlen", dtype="bf16", B=1, Tq=1, Tkv=1, H=H, d=d, rank=R)
+    wts = make_inputs(w0, seed=40)
+    qs, lats = [], []
+    for n, (tq, tkv) in enumerate(case["lens"]):
+        ws = custom_workload("varlen", dtype="bf16", B=1, Tq=tq, Tkv=tkv, H=H, d=d, rank=R)
+        x = make_inputs(ws, seed=41 + n)
+        qs.append(x["q"][0]); lats.append(x["kv_latent"][0])
+    cu_q = [0]; cu_kv = [0]
+    for tq, tkv in case["lens"]:
+        cu_q.append(cu_q[-1] + tq); cu_kv.append(cu_kv[-1] + tkv)
+    q = cuda(torch.cat(qs)); lat = cuda(torch.cat(lats))
+    cq = torch.tensor(cu_q, dtype=torch.int32, device="cuda")
+    ck = torch.tensor(cu_kv, dtype=torch.int32, device="cuda")
+    maxq = max(t for t, _ in case["lens"])
+    scale = w0.scale
+    out = mla.attention_varlen(q, lat, cuda(wts["w_up_k"]), cuda(wts["w_up_v"]), cq, ck, maxq,
+                               scale, case["causal"])
+    outb = mla.attention_varlen(q, lat, cuda(wts["w_up_k"]), cuda(wts["w_up_v"]), cq, ck, maxq,
+                                scale, case["causal"], out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert mla.device_error() == 0
+    for n, (tq, tkv) in enumerate(case["lens"]):
+        ref = oracle.attention(qs[n][None], lats[n][None], wts["w_up_k"], wts["w_up_v"], scale,
+                               case["causal"])[0]
+        got = to_np(out)[cu_q[n]:cu_q[n + 1]]
+        assert_bf16_close(got, ref, f"varlen sequence {n} ({tq},{tkv})")
+        assert_bf16_close(to_np(outb.float())[cu_q[n]:cu_q[n + 1]], ref, f"varlen seq {n} bf16")
+
+
+def test_varlen_bad_lengths_are_reported_not_written():
+    """A sequence whose key range is shorter than its query range is skipped
+    (its rows stay untouched) and recorded in the device error word."""
+    H, d, R = 2, 64, 128
+    w0 = custom_workload("varlen", dtype="bf16", B=1, Tq=40, Tkv=40, H=H, d=d, rank=R)
+    x = make_inputs(w0, seed=50)
+    q = cuda(torch.cat([x["q"][0], x["q"][0]]))
+    lat = cuda(x["kv_latent"][0])
+    cq = torch.tensor([0, 40, 80], dtype=torch.int32, device="cuda")
+    ck = torch.tensor([0, 40, 30], dtype=torch.int32, device="cuda")   # second range is negative
+    out = torch.full((80, H, d), 7.0, device="cuda")
+    assert mla.device_error(clear=True) == 0
+    mla.attention_varlen(q, lat, cuda(x["w_up_k"]), cuda(x["w_up_v"]), cq, ck, 40, w0.scale,
+                         out=out)
+    torch.cuda.synchronize()
+    assert mla.device_error(clear=True) == 0x201
+    assert (out[40:] == 7.0).all()
+    assert torch.isfinite(out[:40]).all() and not (out[:40] == 7.0).all()
