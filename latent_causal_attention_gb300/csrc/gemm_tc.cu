@@ -22,15 +22,29 @@ namespace mla {
 
 namespace {
 
-constexpr int kBM = 128, kBK = 64, kStages = 4, kThreads = 128;
+constexpr int kBM = 128, kBK = 64, kThreads = 128;
 constexpr int kAStage = kBM * kBK * 2;      // 16 KB
-constexpr int kBStage = 256 * kBK * 2;      // 32 KB (BN <= 256)
-constexpr int kSmemBytes = kStages * (kAStage + kBStage) + 256 + 1024;
 
-template <bool kBMN>
+// Tile shapes: BN <= 256 with a 4-stage ring, or BN = 512 (two N = 256 MMAs per
+// K-step into all 512 TMEM columns) with 2 stages, for narrow-M contractions
+// whose whole N fits one CTA (one wave of CTAs instead of two).
+template <bool kWide>
+struct GemmShape {
+  static constexpr int kStages = kWide ? 2 : 4;
+  static constexpr int kBNMax = kWide ? 512 : 256;
+  static constexpr int kBStage = kBNMax * kBK * 2;   // 64 or 32 KB
+  static constexpr int kTmemCols = kWide ? 512 : 256;
+  static constexpr int kSmemBytes = kStages * (kAStage + kBStage) + 256 + 1024;
+};
+
+template <bool kBMN, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB, GemmArgs g) {
+  constexpr int kStages = GemmShape<kWide>::kStages;
+  constexpr int kBStage = GemmShape<kWide>::kBStage;
+  constexpr int kTmemCols = GemmShape<kWide>::kTmemCols;
+  static_assert(!(kWide && kBMN), "BN = 512 is for K-major B");
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -56,7 +70,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbarrier_init_cluster();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 256);
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -74,7 +88,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++issued;
       mbar_arrive_expect_tx(&full[s], bytes);
       tma_load_3d(sA + s * kAStage, &mapA, &full[s], kb * kBK, grp, m0);
-      if (!kBMN) {
+      if (kWide) {                       // two boxes of 256 rows of B
+        tma_load_3d(sB + s * kBStage, &mapB, &full[s], kb * kBK, grp, n0);
+        tma_load_3d(sB + s * kBStage + 256 * 128, &mapB, &full[s], kb * kBK, grp, n0 + 256);
+      } else if (!kBMN) {
         tma_load_3d(sB + s * kBStage, &mapB, &full[s], kb * kBK, grp, n0);
       } else {
         for (int c = 0; c < BN / 64; ++c)
@@ -87,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&full[kb % kStages], (kb / kStages) & 1, 4, nullptr);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = make_idesc_bf16(kBM, BN, false, kBMN);
+    const uint32_t idesc = make_idesc_bf16(kBM, kWide ? 256 : BN, false, kBMN);
     bool ok = true;
     for (int kb = 0; kb < kblocks && ok; ++kb) {
       const int s = kb % kStages;
@@ -101,6 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd = kBMN ? make_sdesc_sw128(b0 + kk * 2048, kBK * 128, 1024)
                                  : make_sdesc_sw128(b0 + kk * 32, 16, 1024);
         umma_bf16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        if (kWide)                       // columns 256..511: B rows 256..511
+          umma_bf16(tmem + 256, ad, bd + (uint64_t)((256 * 128) >> 4), idesc,
+                    (kb | kk) != 0 ? 1u : 0u);
       }
       umma_commit(&empty[s]);
     }
@@ -142,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -156,23 +176,27 @@ cudaError_t gemm_read_device_error(unsigned int* code, int clear) {
   return e;
 }
 
+template <bool kBMN, bool kWide>
+static cudaError_t launch_shape(const CUtensorMap& mapA, const CUtensorMap& mapB,
+                                const GemmArgs& args, cudaStream_t stream) {
+  dim3 grid(args.N / args.BN, (args.M + kBM - 1) / kBM, args.G);
+  auto k = gemm_tc_kernel<kBMN, kWide>;
+  constexpr int smem = GemmShape<kWide>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, smem, stream>>>(mapA, mapB, args);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_tc(const CUtensorMap& mapA, const CUtensorMap& mapB, bool b_mn_major,
                            const GemmArgs& args, cudaStream_t stream) {
-  dim3 grid(args.N / args.BN, (args.M + kBM - 1) / kBM, args.G);
-  if (b_mn_major) {
-    auto k = gemm_tc_kernel<true>;
-    cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, args);
-  } else {
-    auto k = gemm_tc_kernel<false>;
-    cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, args);
+  if (args.BN == 512) {
+    if (b_mn_major) return cudaErrorInvalidValue;
+    return launch_shape<false, true>(mapA, mapB, args, stream);
   }
-  return cudaGetLastError();
+  if (args.BN > 256) return cudaErrorInvalidValue;
+  return b_mn_major ? launch_shape<true, false>(mapA, mapB, args, stream)
+                    : launch_shape<false, false>(mapA, mapB, args, stream);
 }
 
 }  // namespace mla

@@ -28,7 +28,7 @@ cudaError_t launch_projection_cuda_core(const void* hidden, const void* w_down,
 //   C: element (g, m, n) at C + g*c_gs + m*c_rs + n, fp32 or bf16.
 struct GemmArgs {
   int M, N, K, G;
-  int BN;            // 64, 128 or 256; divides N
+  int BN;            // 64, 128, 256 (divides N) or 512 (= N, K-major B, B box 256 rows)
   float alpha;
   void* C;
   int c_bf16;

@@ -364,6 +364,9 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
     return MLA_ERR_CUDA;
   GemmArgs g = {};
   g.M = (int)BT; g.N = R; g.K = d; g.G = H; g.BN = bn_abs;
+  // one query row block per head (decode): the whole rank in one CTA, so the
+  // heads' tiles run in one wave
+  if (R == 512 && BT <= 128) g.BN = 512;
   g.alpha = scale * 1.4426950408889634f;
   g.C = qp; g.c_bf16 = 1; g.c_rs = (int64_t)H * R; g.c_gs = R;
   if (staged(0, stream, [&] { return launch_gemm_tc(mA, mB, false, g, stream); }) != cudaSuccess)
