@@ -449,6 +449,51 @@ def run_ours(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+def run_decode_only(args):
+    """Only the decode attention (B64, one query over 4096 latent rows, H128,
+    rank 512): warm-up, then timed calls with the L2 flushed between them; one
+    JSON line.  A small driver for profiling the decode kernels."""
+    import torch
+
+    import latent_causal_attention_gb300 as mla
+    from latent_causal_attention_gb300.build import build
+    from latent_causal_attention_gb300.inputs import WORKLOADS, make_inputs
+
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    wd = WORKLOADS["decode_bf16"]
+    xd = {k: v.to(dev) for k, v in make_inputs(wd).items()}
+    outd = torch.empty(wd.B, wd.Tq, wd.H, wd.d, device=dev, dtype=torch.float32)
+    wsd = torch.empty(max(1, mla.workspace_size(wd.B, wd.Tq, wd.Tkv, wd.H, wd.d, wd.rank,
+                                                torch.bfloat16)), device=dev, dtype=torch.uint8)
+    flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def dstep():
+        mla.attention(xd["q"], xd["kv_latent"], xd["w_up_k"], xd["w_up_v"], wd.scale, True,
+                      out=outd, workspace=wsd)
+
+    for _ in range(args.warmup):
+        dstep()
+    s_ = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_ = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        s_[k].record(stream)
+        dstep()
+        e_[k].record(stream)
+    torch.cuda.synchronize()
+    dms = statistics.mean(a.elapsed_time(b) for a, b in zip(s_, e_))
+    nbytes = wd.attention_bytes(out_bytes=4)
+    print(json.dumps({"mode": "decode-only", "workload": "decode_bf16", "ms": round(dms, 4),
+                      "GB_per_s": round(nbytes / (dms * 1e-3) / 1e9, 1),
+                      "frac_hbm": round(nbytes / (dms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                      "steps": args.steps, "warmup": args.warmup}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,9 +503,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-explicit", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode attention (a driver for profiling its kernels)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.decode_only:
+        run_decode_only(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
