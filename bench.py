@@ -33,6 +33,25 @@ METRIC = "latent-attention TFLOP/s and HBM GB/s on 1 GB300; fraction of roofline
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    one all_reduce(MAX) of a scalar, outside the timed regions."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: float, steps: int, world: int, max_ms: float,
+                   scale: float = 1e12) -> float:
+    """Whole-job rate: every rank processes its own copy of the workload (weak
+    scaling), so the job does world * units per step, over the slowest rank's time."""
+    return world * units_per_rank_step * steps / (max_ms * 1e-3) / scale
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -255,12 +274,9 @@ def run_ours(args, rank: int, world: int):
     stage_ids = [(4, "projection"), (1, "attention_fused")] if fused else \
         [(4, "projection"), (0, "absorb"), (1, "flash"), (3, "v_up")]
     stages = {name: statistics.mean(e.elapsed_ms(i) for e in ev) for i, name in stage_ids}
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops_step, args.steps, world, total_ms)
 
     # --- end to end: pinned host inputs -> device -> path -> host result.
     # Every step copies its inputs from pinned host memory and its result back.
@@ -317,11 +333,8 @@ def run_ours(args, rank: int, world: int):
 
     e2e_run(2)
     e2e_ms = e2e_run(e2e_steps)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = job_throughput(flops_step, e2e_steps, world, e2e_ms)
 
     # --- decode workload (bandwidth-bound): GB/s of algorithmic bytes
     dec = None
