@@ -370,3 +370,16 @@ def test_varlen_bad_lengths_are_reported_not_written():
     assert mla.device_error(clear=True) == 0x201
     assert (out[40:] == 7.0).all()
     assert torch.isfinite(out[:40]).all() and not (out[:40] == 7.0).all()
+
+
+def test_explicit_attention_prefill_size_sampled():
+    """The comparator kernel at the prefill size (B2 T4096 H32 d128), sampled
+    query rows (all heads) against the float64 attention over the same k, v."""
+    w = custom_workload("explicit_prefill", dtype="bf16", B=2, Tq=4096, Tkv=4096, H=32, d=128,
+                        rank=64)
+    x = make_kv_inputs(w, seed=61)
+    out = mla.explicit_attention(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), w.scale, True)
+    torch.cuda.synchronize()
+    rows = [0, 127, 128, 2049, 4095]
+    ref = explicit.attention_kv(x["q"], x["k"], x["v"], w.scale, True, query_rows=rows)
+    assert_bf16_close(to_np(out)[:, rows], ref, "explicit prefill sampled rows")
