@@ -336,8 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // p and tiles j = p (mod 2).  A thread that has just issued MMAs waits for
     // the tensor core to take them before its next barrier test completes;
     // with two issuers the other one keeps the tensor core fed meanwhile.
-    // O_lat was zeroed by the softmax warps, so every P.L accumulates and the
-    // order in which the two issuers' O MMAs reach the tensor core is free.
+    // O_lat was zeroed by the softmax warps, so every P.L accumulates.
     // Per tile j, the four long O(j) += P(j) L(j) MMAs (N = RC) are interleaved
     // with the narrow S(j+2) = q' L(j+2)^T MMAs (N = 64) of the same issuer,
     // fully unrolled with descriptors advanced by constants.
@@ -388,7 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool s_ready =
             js < nt && mbar_test(smem_u32(&bars->l_full[js % kStages]), (js / kStages) & 1) &&
             mbar_test(smem_u32(&bars->s_empty[par]), ((js >> 1) & 1) ^ 1);
-        const bool o_ready = jo < js && mbar_test(smem_u32(&bars->p_full[par]), (jo >> 1) & 1);
+        // O(jo) also waits for O(jo-1) (the other issuer's) to complete, so the
+        // P.L products accumulate in tile order: the result does not depend on
+        // how the two issuers' instructions interleave
+        const bool o_ready =
+            jo < js && mbar_test(smem_u32(&bars->p_full[par]), (jo >> 1) & 1) &&
+            (jo == 0 || mbar_test(smem_u32(&bars->p_empty[par ^ 1]), ((jo - 1) >> 1) & 1));
         if (!s_ready && !o_ready) {
           // back off: this warp shares an SM sub-partition with softmax warps
           __nanosleep(32);

@@ -383,3 +383,27 @@ def test_explicit_attention_prefill_size_sampled():
     rows = [0, 127, 128, 2049, 4095]
     ref = explicit.attention_kv(x["q"], x["k"], x["v"], w.scale, True, query_rows=rows)
     assert_bf16_close(to_np(out)[:, rows], ref, "explicit prefill sampled rows")
+
+
+def test_two_streams_run_independent_calls(oracle):
+    """Calls on two CUDA streams at once (each with its own workspace and
+    output) give the same results as one at a time: no hidden shared state."""
+    shapes = [custom_workload("s1", dtype="bf16", B=2, Tq=1, Tkv=700, H=16, d=64, rank=512),
+              custom_workload("s2", dtype="bf16", B=1, Tq=256, Tkv=256, H=4, d=128, rank=512)]
+    xs = [{k: cuda(v) for k, v in make_inputs(w, seed=70 + n).items()}
+          for n, w in enumerate(shapes)]
+    refs = [mla.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale)
+            for x, w in zip(xs, shapes)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in shapes]
+    outs = []
+    for _ in range(3):
+        outs = []
+        for x, w, s in zip(xs, shapes, streams):
+            with torch.cuda.stream(s):
+                outs.append(mla.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"],
+                                          w.scale))
+        torch.cuda.synchronize()
+        for o, r in zip(outs, refs):
+            assert torch.equal(o, r)
+    assert mla.device_error() == 0
