@@ -340,33 +340,8 @@ def run_ours(args, rank: int, world: int):
     dec = None
     if not args.no_decode:
         wd = WORKLOADS["decode_bf16"]
-        xd = {k: v.to(dev) for k, v in make_inputs(wd).items()}
-        outd = torch.empty(wd.B, wd.Tq, wd.H, wd.d, device=dev, dtype=torch.float32)
-        wsd = torch.empty(max(1, mla.workspace_size(wd.B, wd.Tq, wd.Tkv, wd.H, wd.d, wd.rank,
-                                                    torch.bfloat16)), device=dev,
-                          dtype=torch.uint8)
-
-        def dstep():
-            mla.attention(xd["q"], xd["kv_latent"], xd["w_up_k"], xd["w_up_v"], wd.scale, True,
-                          out=outd, workspace=wsd)
-
-        for _ in range(max(3, args.warmup)):
-            dstep()
-        n = max(10, args.steps)
-        dev_ev = [mla.StageEvents() for _ in range(n)]
-        s_ = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        e_ = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        torch.cuda.synchronize()
-        for k in range(n):
-            flush.zero_()
-            dev_ev[k].install()
-            s_[k].record(stream)
-            dstep()
-            e_[k].record(stream)
-        torch.cuda.synchronize()
-        mla.StageEvents.uninstall()
-        dms = statistics.mean(a.elapsed_time(b) for a, b in zip(s_, e_))
-        dflash = statistics.mean(e.elapsed_ms(1) for e in dev_ev)
+        dms, dflash = time_attention_only(wd, dev, flush, stream, max(10, args.steps),
+                                          max(3, args.warmup))
         nbytes = wd.attention_bytes(out_bytes=4)
         dec = {"workload": "decode_bf16: B64, one query at t=4095 over 4096 latent rows, H128 d128 "
                            "rank512, bf16 in, fp32 out",
@@ -377,6 +352,20 @@ def run_ours(args, rank: int, world: int):
                "flash_ms": round(dflash, 4),
                "flash_frac_hbm": round(268435456 * 1.0 / (dflash * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                        4)}
+
+    # --- the mid-size prefill workload (rank 256: one CTA per row block, no
+    # CTA pair): TFLOP/s of the whole attention, one fused kernel
+    mid = None
+    if not args.no_mid:
+        wm = WORKLOADS["mid_bf16"]
+        mms, mflash = time_attention_only(wm, dev, flush, stream, max(10, args.steps),
+                                          max(3, args.warmup))
+        mid = {"workload": "mid_bf16: causal latent attention B4 T1024 H16 d64 rank256, bf16 in, "
+                           "fp32 out",
+               "ms": round(mms, 4), "kernel_ms": round(mflash, 4),
+               "TFLOP_per_s": round(wm.attention_flops() / (mms * 1e-3) / 1e12, 2),
+               "frac_peak": round(wm.attention_flops() / (mms * 1e-3) / 1e12
+                                  / peaks["bf16_tflops"], 4)}
 
     # --- comparator: the same prefill step with k and v materialised (projection
     # with w_up_k / w_up_v outputs, then attention over explicit k, v)
@@ -455,6 +444,7 @@ def run_ours(args, rank: int, world: int):
         "gpu_launches": int(launches),
         "clocks": clocks,
         "decode": dec,
+        "mid": mid,
         "explicit_kv_comparator": expl,
     }
     if cpu_val is not None:
@@ -462,48 +452,68 @@ def run_ours(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
-def run_decode_only(args):
-    """Only the decode attention (B64, one query over 4096 latent rows, H128,
-    rank 512): warm-up, then timed calls with the L2 flushed between them; one
-    JSON line.  A small driver for profiling the decode kernels."""
+def time_attention_only(w, dev, flush, stream, n: int, warmup: int):
+    """Mean CUDA-event time (ms) of one attention call on workload w with its
+    inputs resident and the L2 flushed before every call (outside the events),
+    and the mean time of its main attention kernel (library stage events)."""
     import torch
 
     import latent_causal_attention_gb300 as mla
+    from latent_causal_attention_gb300.inputs import make_inputs
+
+    x = {k: v.to(dev) for k, v in make_inputs(w).items()}
+    out = torch.empty(w.B, w.Tq, w.H, w.d, device=dev, dtype=torch.float32)
+    ws = torch.empty(max(1, mla.workspace_size(w.B, w.Tq, w.Tkv, w.H, w.d, w.rank,
+                                               torch.bfloat16)), device=dev, dtype=torch.uint8)
+
+    def call():
+        mla.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale, True,
+                      out=out, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    evs = [mla.StageEvents() for _ in range(n)]
+    s_ = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    e_ = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    torch.cuda.synchronize()
+    for k in range(n):
+        flush.zero_()
+        evs[k].install()
+        s_[k].record(stream)
+        call()
+        e_[k].record(stream)
+    torch.cuda.synchronize()
+    mla.StageEvents.uninstall()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in zip(s_, e_))
+    kernel_ms = statistics.mean(e.elapsed_ms(1) for e in evs)
+    return ms, kernel_ms
+
+
+def run_attention_only(args, name: str):
+    """Only one workload's attention (decode_bf16 or mid_bf16): warm-up, then
+    timed calls with the L2 flushed between them; one JSON line.  A small
+    driver for profiling that workload's kernels."""
+    import torch
+
     from latent_causal_attention_gb300.build import build
-    from latent_causal_attention_gb300.inputs import WORKLOADS, make_inputs
+    from latent_causal_attention_gb300.inputs import WORKLOADS
 
     build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peaks, _ = load_peaks()
-    wd = WORKLOADS["decode_bf16"]
-    xd = {k: v.to(dev) for k, v in make_inputs(wd).items()}
-    outd = torch.empty(wd.B, wd.Tq, wd.H, wd.d, device=dev, dtype=torch.float32)
-    wsd = torch.empty(max(1, mla.workspace_size(wd.B, wd.Tq, wd.Tkv, wd.H, wd.d, wd.rank,
-                                                torch.bfloat16)), device=dev, dtype=torch.uint8)
+    w = WORKLOADS[name]
     flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream(dev)
-
-    def dstep():
-        mla.attention(xd["q"], xd["kv_latent"], xd["w_up_k"], xd["w_up_v"], wd.scale, True,
-                      out=outd, workspace=wsd)
-
-    for _ in range(args.warmup):
-        dstep()
-    s_ = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e_ = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for k in range(args.steps):
-        flush.zero_()
-        s_[k].record(stream)
-        dstep()
-        e_[k].record(stream)
-    torch.cuda.synchronize()
-    dms = statistics.mean(a.elapsed_time(b) for a, b in zip(s_, e_))
-    nbytes = wd.attention_bytes(out_bytes=4)
-    print(json.dumps({"mode": "decode-only", "workload": "decode_bf16", "ms": round(dms, 4),
-                      "GB_per_s": round(nbytes / (dms * 1e-3) / 1e9, 1),
-                      "frac_hbm": round(nbytes / (dms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+    ms, kernel_ms = time_attention_only(w, dev, flush, stream, args.steps, args.warmup)
+    nbytes = w.attention_bytes(out_bytes=4)
+    tflops = w.attention_flops() / (ms * 1e-3) / 1e12
+    print(json.dumps({"mode": "attention-only", "workload": name, "ms": round(ms, 4),
+                      "kernel_ms": round(kernel_ms, 4),
+                      "GB_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                      "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                      "TFLOP_per_s": round(tflops, 2),
+                      "frac_peak": round(tflops / peaks["bf16_tflops"], 4),
                       "steps": args.steps, "warmup": args.warmup}), flush=True)
 
 
@@ -516,13 +526,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-explicit", action="store_true")
+    ap.add_argument("--no-mid", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode attention (a driver for profiling its kernels)")
+    ap.add_argument("--mid-only", action="store_true",
+                    help="time only the mid-size attention (a driver for profiling its kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.decode_only:
-        run_decode_only(args)
+    if args.decode_only or args.mid_only:
+        run_attention_only(args, "decode_bf16" if args.decode_only else "mid_bf16")
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -68,11 +68,38 @@ constexpr int kBarBytes = 512;
 constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "dynamic shared memory limit");
 
-// fused prefill staging inside the latent ring (before / after the loop):
-//   prologue: q tile at 0 (d/64 x 16 KB), w_up_k rows at 32 KB (d/64 x RC*128 B)
-//   epilogue: O_lat bf16 at 0 (RC/64 x 16 KB), w_up_v rows at 64 KB (d/64 x RC*128 B)
-constexpr int kFusedWkOff = 32 * 1024;
-constexpr int kFusedWvOff = 64 * 1024;
+// Fused prefill staging (d <= 128, RC <= 256).  Prologue: the q tile (d/64 x
+// 16 KB) in the P buffers and this CTA's w_up_k rows (d/64 x RC*128 B) in the
+// receive buffers, both free until q' is in TMEM, so the latent ring starts at
+// once.  Epilogue, inside the latent ring: w_up_v rows (d/64 x RC*128 B) in the
+// stages that tiles nt and nt+1 would take (free as soon as P.L of tiles nt-4
+// and nt-3 has completed, so the load overlaps the end of the loop) and the
+// normalised O_lat (bf16, RC/64 x 16 KB) in the stages of tiles nt-2 and nt-1.
+static_assert(2 * kRows * 128 <= 2 * kPBytes, "q tile staging");
+static_assert(2 * kMaxRC * 128 <= kXBuf * kXBytes, "w_up_k staging");
+static_assert(kMaxRC * 128 <= kLStage && 2 * kRows * 128 <= kLStage, "epilogue staging");
+
+struct EpiStages {
+  uint32_t wv_lo;    // stage of w_up_v chunk 0 (d columns 0..63)
+  uint32_t wv_lbo;   // byte distance to chunk 1 (d columns 64..127)
+  uint32_t o_a;      // stage of O_lat chunks 0, 1 (rank columns 0..127)
+  uint32_t o_b;      // stage of O_lat chunks 2, 3
+};
+
+__device__ __forceinline__ EpiStages epi_stages(int nt, int dch) {
+  const uint32_t s0 = (uint32_t)(nt % kStages), s1 = (uint32_t)((nt + 1) % kStages);
+  EpiStages e;
+  e.wv_lo = dch > 1 ? min(s0, s1) : s0;
+  e.wv_lbo = dch > 1 ? (max(s0, s1) - min(s0, s1)) * (uint32_t)kLStage : (uint32_t)kLStage;
+  e.o_a = (uint32_t)((nt + 2) % kStages);
+  e.o_b = (uint32_t)((nt + 3) % kStages);
+  return e;
+}
+
+// Shared-memory byte offset of 16 KB O_lat chunk c (64 rank columns x 128 rows).
+__device__ __forceinline__ uint32_t epi_o_chunk(const EpiStages& e, uint32_t c) {
+  return (c < 2 ? e.o_a : e.o_b) * (uint32_t)kLStage + (c & 1u) * (uint32_t)(kRows * 128);
+}
 
 constexpr uint32_t kTmemO = 0;       // columns [0, RC)
 constexpr uint32_t kTmemS = 256;     // two 64-column S buffers at 256, 320
@@ -163,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     flash_packed_kernel(const __grid_constant__ CUtensorMap mapQ,
                         const __grid_constant__ CUtensorMap mapL,
                         const __grid_constant__ CUtensorMap mapWk,
-                        const __grid_constant__ CUtensorMap mapWv, FlashArgs a) {
+                        const __grid_constant__ CUtensorMap mapWv,
+                        const __grid_constant__ CUtensorMap mapO, FlashArgs a) {
   extern __shared__ uint8_t flash_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(flash_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -265,17 +293,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&mapQ);
       prefetch_tensormap(&mapL);
       if constexpr (kFused) {
-        // q tile (128 positions x d of one head) and this CTA's rows of w_up_k
-        // into latent stages 0-2; the latent ring starts once they are consumed.
+        // q tile (128 positions x d of one head) into the P buffers and this
+        // CTA's rows of w_up_k into the receive buffers; the latent ring
+        // starts at once
         const int dch = a.d / 64;
         mbar_arrive_expect_tx(&bars->pro_full, (uint32_t)(kRows * a.d * 2 + RC * a.d * 2));
         for (int kc = 0; kc < dch; ++kc) {
-          tma_load_3d(sL + kc * (kRows * 128), &mapQ, &bars->pro_full, 64 * kc, head,
+          tma_load_3d(sP + kc * (kRows * 128), &mapQ, &bars->pro_full, 64 * kc, head,
                       q0 + row0);
-          tma_load_3d(sL + kFusedWkOff + kc * (RC * 128), &mapWk, &bars->pro_full, 64 * kc, head,
-                      c0);
+          tma_load_3d(sX + kc * (RC * 128), &mapWk, &bars->pro_full, 64 * kc, head, c0);
         }
-        mbar_wait(&bars->pro_done, 0, 13, abort_flag);
       } else if constexpr (kExplicit) {
         // q tile (128 positions x d of one head) into the staging area
         mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRows * RC * 2));
@@ -314,14 +341,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = max(0, issued - kStages); j < issued; ++j)
         mbar_wait(&bars->l_full[j % kStages], (j / kStages) & 1, 11, nullptr);
       if constexpr (kFused) {
-        // w_up_v rows of this CTA (MN-major B of the output MMA) once the last
-        // P.L has finished reading the latent stages
-        if (mbar_wait(&bars->o_last, 0, 14, abort_flag)) {
-          const int dch = a.d / 64;
+        // w_up_v rows of this CTA (MN-major B of the output MMA) into the ring
+        // stages that tiles nt and nt+1 would take, as soon as they are free
+        const int dch = a.d / 64;
+        const EpiStages es = epi_stages(nt, dch);
+        mbar_wait(&bars->pro_full, 0, 13, nullptr);     // the prologue copies have landed
+        bool okw = issued == nt;
+        for (int nc = 0; nc < dch && okw; ++nc)
+          okw = mbar_wait(&bars->l_empty[(nt + nc) % kStages],
+                          (((nt + nc) / kStages) & 1) ^ 1, 14, abort_flag);
+        if (okw) {
           mbar_arrive_expect_tx(&bars->epi_w, (uint32_t)(RC * a.d * 2));
           for (int nc = 0; nc < dch; ++nc)
             for (int kb = 0; kb < RC / 64; ++kb)
-              tma_load_3d(sL + kFusedWvOff + nc * (RC * 128) + kb * (64 * 128), &mapWv,
+              tma_load_3d(sL + es.wv_lo * kLStage + nc * es.wv_lbo + kb * (64 * 128), &mapWv,
                           &bars->epi_w, 64 * nc, head, c0 + 64 * kb);
           mbar_wait(&bars->epi_w, 0, 15, nullptr);
         }
@@ -356,8 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (ok) {
             constexpr uint32_t idesc_q = make_idesc_bf16(kRows, kRC, false, false);
-            const uint64_t aq = make_sdesc_sw128(l0, 16, 1024);
-            const uint64_t bw = make_sdesc_sw128(l0 + kFusedWkOff, 16, 1024);
+            const uint64_t aq = make_sdesc_sw128(p0, 16, 1024);
+            const uint64_t bw = make_sdesc_sw128(smem_u32(sX), 16, 1024);
             for (int k = 0; k < a.d / 16; ++k)
               umma_bf16(tmem + kTmemO,
                         aq + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
@@ -441,12 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_wait(&bars->epi_w, 0, 26, abort_flag)) {
             tc_fence_after();
             const uint32_t idesc_v = make_idesc_bf16(kRows, a.d, false, true);
-            const uint64_t ao = make_sdesc_sw128(l0, 16, 1024);
-            const uint64_t bv = make_sdesc_sw128(l0 + kFusedWvOff, kRC * 128, 1024);
+            const EpiStages es = epi_stages(nt, a.d / 64);
+            const uint64_t bv = make_sdesc_sw128(l0 + es.wv_lo * kLStage, es.wv_lbo, 1024);
 #pragma unroll
             for (int k = 0; k < kRC / 16; ++k)
               umma_bf16(tmem + kTmemS,
-                        ao + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
+                        make_sdesc_sw128(l0 + epi_o_chunk(es, (uint32_t)(k >> 2)) + (k & 3) * 32,
+                                         16, 1024),
                         bv + (uint64_t)((k * 2048) >> 4), idesc_v, k > 0 ? 1u : 0u);
           }
           umma_commit(&bars->epi_done);
@@ -718,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // normalised O_lat (bf16) -> shared memory, the A operand of the output MMA
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       const uint32_t a0s = smem_u32(sL);
+      const EpiStages es = epi_stages(nt, a.d / 64);
       for (int c = oc0; c < oc0 + RC / 2; c += 32) {
         float o[32];
         if (have_o) {
@@ -727,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0.f;
         }
-        const uint32_t base = a0s + (uint32_t)(c >> 6) * (kRows * 128);
+        const uint32_t base = a0s + epi_o_chunk(es, (uint32_t)(c >> 6));
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           st_shared_v4(base + sw128_offset((uint32_t)r, (uint32_t)(((c & 63) >> 3) + q)),
@@ -748,6 +783,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool have_peer = true;
       if (a.pair) have_peer = have_out && warp_wait<true>(&bars->epi_x, 0, 37, abort_flag);
       const int64_t orow = (((int64_t)q0 + grow) * a.H + head) * a.d;
+      // A full 128-row block leaves as tile stores of 128 x 128-byte boxes,
+      // staged (128-byte swizzle) in the latent ring, which the output MMA no
+      // longer reads; the rows of a partial block, or a column range narrower
+      // than one box, are written one by one.
+      const int box_cols = a.out_bf16 ? 64 : 32;
+      const bool tile_store = row0 + kRows <= rows_b && dh % box_cols == 0;
+      const int cbase = a.pair ? (int)crank * dh : 0;        // first column stored here
+      const uint32_t stage0 = smem_u32(sL);
       for (int c = cfirst; c < cfirst + dh / 2; c += 16) {
         float v[16];
         if (have_out) {
@@ -771,7 +814,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[4 * q + 3] += x3;
           }
         }
-        if (row_valid && have_peer) {
+        if (tile_store) {
+          const int cr = c - cbase;
+          const uint32_t box = stage0 + (uint32_t)(cr / box_cols) * (kRows * 128);
+          if (a.out_bf16) {
+            const uint32_t ch = (uint32_t)((cr % 64) >> 3);      // 16 columns = 2 chunks
+            st_shared_v4(box + sw128_offset((uint32_t)r, ch), pack_bf16x2(v[0], v[1]),
+                         pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                         pack_bf16x2(v[6], v[7]));
+            st_shared_v4(box + sw128_offset((uint32_t)r, ch + 1), pack_bf16x2(v[8], v[9]),
+                         pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                         pack_bf16x2(v[14], v[15]));
+          } else {
+            const uint32_t ch = (uint32_t)((cr % 32) >> 2);      // 16 columns = 4 chunks
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(box + sw128_offset((uint32_t)r, ch + (uint32_t)q),
+                           __float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                           __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+          }
+        } else if (row_valid && have_peer) {
           if (a.out_bf16) {
             uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + c);
             d4[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
@@ -784,6 +846,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 4; ++q)
               d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           }
+        }
+      }
+      if (tile_store) {
+        // all eight softmax warps have staged their columns: one thread stores
+        fence_proxy_async_smem();
+        named_bar_sync(5, 256);
+        if (warp == 6 && lane == 0 && have_peer) {
+          for (int bx = 0; bx < dh / box_cols; ++bx)
+            tma_store_3d(&mapO, stage0 + (uint32_t)bx * (kRows * 128), cbase + bx * box_cols,
+                         head, q0 + row0);
+          bulk_commit_group();
+          bulk_wait_read_all();     // the staging must outlive the reads, not the writes
         }
       }
     } else if constexpr (kExplicit) {
@@ -945,7 +1019,8 @@ cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, cudaStream_t 
 template <int kRC, int kMode>
 static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                   const CUtensorMap& mapWk, const CUtensorMap& mapWv,
-                                  const FlashArgs& args, cudaStream_t stream) {
+                                  const CUtensorMap& mapO, const FlashArgs& args,
+                                  cudaStream_t stream) {
   auto kern = flash_packed_kernel<kRC, kMode>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -965,7 +1040,7 @@ static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& m
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, args);
+  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, mapO, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -973,22 +1048,27 @@ static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& m
 cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                 const FlashArgs& args, cudaStream_t stream) {
   switch (args.RC) {
-    case 64: return launch_flash_rc<64, kModePacked>(mapQ, mapL, mapQ, mapQ, args, stream);
-    case 128: return launch_flash_rc<128, kModePacked>(mapQ, mapL, mapQ, mapQ, args, stream);
-    case 192: return launch_flash_rc<192, kModePacked>(mapQ, mapL, mapQ, mapQ, args, stream);
-    case 256: return launch_flash_rc<256, kModePacked>(mapQ, mapL, mapQ, mapQ, args, stream);
+    case 64: return launch_flash_rc<64, kModePacked>(mapQ, mapL, mapQ, mapQ, mapQ, args, stream);
+    case 128: return launch_flash_rc<128, kModePacked>(mapQ, mapL, mapQ, mapQ, mapQ, args, stream);
+    case 192: return launch_flash_rc<192, kModePacked>(mapQ, mapL, mapQ, mapQ, mapQ, args, stream);
+    case 256: return launch_flash_rc<256, kModePacked>(mapQ, mapL, mapQ, mapQ, mapQ, args, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                const CUtensorMap& mapWk, const CUtensorMap& mapWv,
-                               const FlashArgs& args, cudaStream_t stream) {
+                               const CUtensorMap& mapO, const FlashArgs& args,
+                               cudaStream_t stream) {
   switch (args.RC) {
-    case 64: return launch_flash_rc<64, kModeFused>(mapQ, mapL, mapWk, mapWv, args, stream);
-    case 128: return launch_flash_rc<128, kModeFused>(mapQ, mapL, mapWk, mapWv, args, stream);
-    case 192: return launch_flash_rc<192, kModeFused>(mapQ, mapL, mapWk, mapWv, args, stream);
-    case 256: return launch_flash_rc<256, kModeFused>(mapQ, mapL, mapWk, mapWv, args, stream);
+    case 64:
+      return launch_flash_rc<64, kModeFused>(mapQ, mapL, mapWk, mapWv, mapO, args, stream);
+    case 128:
+      return launch_flash_rc<128, kModeFused>(mapQ, mapL, mapWk, mapWv, mapO, args, stream);
+    case 192:
+      return launch_flash_rc<192, kModeFused>(mapQ, mapL, mapWk, mapWv, mapO, args, stream);
+    case 256:
+      return launch_flash_rc<256, kModeFused>(mapQ, mapL, mapWk, mapWv, mapO, args, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -997,8 +1077,10 @@ cudaError_t launch_flash_explicit(const CUtensorMap& mapQ, const CUtensorMap& ma
                                   const CUtensorMap& mapV, const FlashArgs& args,
                                   cudaStream_t stream) {
   switch (args.RC) {
-    case 64: return launch_flash_rc<64, kModeExplicit>(mapQ, mapK, mapV, mapV, args, stream);
-    case 128: return launch_flash_rc<128, kModeExplicit>(mapQ, mapK, mapV, mapV, args, stream);
+    case 64:
+      return launch_flash_rc<64, kModeExplicit>(mapQ, mapK, mapV, mapV, mapQ, args, stream);
+    case 128:
+      return launch_flash_rc<128, kModeExplicit>(mapQ, mapK, mapV, mapV, mapQ, args, stream);
     default: return cudaErrorInvalidValue;
   }
 }

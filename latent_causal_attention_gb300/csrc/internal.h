@@ -68,7 +68,9 @@ cudaError_t launch_flash_packed(const CUtensorMap& mapQ, const CUtensorMap& mapL
                                 const FlashArgs& args, cudaStream_t stream);
 
 // Fused prefill: q (3-D map {d, H, B*Tq}, box {64,1,128}), latent, w_up_k
-// (K-major, {d, H, R}, box {64,1,RC}), w_up_v (MN-major, {d, H, R}, box {64,1,64}).
+// (K-major, {d, H, R}, box {64,1,RC}), w_up_v (MN-major, {d, H, R}, box {64,1,64}),
+// out ({d, H, B*Tq} or {d, H, total_q}, 128-byte swizzle, box {128/elem bytes, 1,
+// 128}; the tile store of full 128-row blocks).
 // Explicit K/V attention: mapQ over q {d, H, B*Tq}, mapK / mapV over k, v
 // {d, H, B*Tkv}; args.RC = args.d (64 or 128), no CTA pair.
 cudaError_t launch_flash_explicit(const CUtensorMap& mapQ, const CUtensorMap& mapK,
@@ -76,7 +78,8 @@ cudaError_t launch_flash_explicit(const CUtensorMap& mapQ, const CUtensorMap& ma
                                   cudaStream_t stream);
 cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                const CUtensorMap& mapWk, const CUtensorMap& mapWv,
-                               const FlashArgs& args, cudaStream_t stream);
+                               const CUtensorMap& mapO, const FlashArgs& args,
+                               cudaStream_t stream);
 
 cudaError_t launch_merge_partials(const float* m_l, int ml_stride, const float* l, const float* o,
                                   void* out, int parts, int rows, int width, int out_bf16,

@@ -53,6 +53,14 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t d
   return r == CUDA_SUCCESS;
 }
 
+// The fused kernel's output tiles: out (rows, H, d) fp32 or bf16 as {d, H, rows},
+// 128-byte swizzled boxes of 128 bytes x 1 head x 128 rows.
+static bool make_out_tmap(CUtensorMap* map, void* out, bool bf16, int d, int H, uint64_t rows) {
+  const int es = bf16 ? 2 : 4;
+  return make_tmap_3d(map, out, es, (uint64_t)d, (uint64_t)H, rows, (uint64_t)d * es,
+                      (uint64_t)H * d * es, 128u / es, 1, 128, true);
+}
+
 // ---------------------------------------------------------------------------
 // Options
 // ---------------------------------------------------------------------------
@@ -326,7 +334,7 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
   const int64_t BT = (int64_t)B * Tq;
   if (p.fused) {
     // one kernel: q . w_up_k -> flash loop over the latent -> . w_up_v -> out
-    CUtensorMap mQ, mL, mWk, mWv;
+    CUtensorMap mQ, mL, mWk, mWv, mO;
     if (!make_tmap_3d(&mQ, q, 2, d, H, BT, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 128,
                       true) ||
         !make_tmap_3d(&mL, kv_latent, 2, R, Tkv, B, (uint64_t)R * 2, (uint64_t)Tkv * R * 2, 64, 64,
@@ -334,14 +342,16 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
         !make_tmap_3d(&mWk, w_up_k, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1,
                       p.RC, true) ||
         !make_tmap_3d(&mWv, w_up_v, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 64,
-                      true))
+                      true) ||
+        !make_out_tmap(&mO, out, out_dtype == MLA_BF16, d, H, (uint64_t)BT))
       return MLA_ERR_CUDA;
     FlashArgs fa = {};
     fa.B = B; fa.Tq = Tq; fa.Tkv = Tkv; fa.H = H; fa.R = R; fa.RC = p.RC; fa.pair = p.pair;
     fa.row_blocks = p.row_blocks; fa.splits = 1; fa.causal = causal ? 1 : 0;
     fa.d = d; fa.qscale = scale * 1.4426950408889634f; fa.out = out;
     fa.out_bf16 = out_dtype == MLA_BF16;
-    if (staged(1, stream, [&] { return launch_flash_fused(mQ, mL, mWk, mWv, fa, stream); }) !=
+    if (staged(1, stream,
+               [&] { return launch_flash_fused(mQ, mL, mWk, mWv, mO, fa, stream); }) !=
         cudaSuccess)
       return MLA_ERR_CUDA;
     return MLA_OK;
@@ -437,7 +447,7 @@ mla_status_t mla_latent_attention_varlen(const void* q, const void* kv_latent, c
   const int R = rank;
   const int pair = R > 256 ? 1 : 0;
   const int RC = pair ? R / 2 : R;
-  CUtensorMap mQ, mL, mWk, mWv;
+  CUtensorMap mQ, mL, mWk, mWv, mO;
   if (!make_tmap_3d(&mQ, q, 2, d, H, (uint64_t)total_q, (uint64_t)d * 2, (uint64_t)H * d * 2, 64,
                     1, 128, true) ||
       !make_tmap_3d(&mL, kv_latent, 2, R, (uint64_t)total_kv, 1, (uint64_t)R * 2,
@@ -445,7 +455,8 @@ mla_status_t mla_latent_attention_varlen(const void* q, const void* kv_latent, c
       !make_tmap_3d(&mWk, w_up_k, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, RC,
                     true) ||
       !make_tmap_3d(&mWv, w_up_v, 2, d, H, R, (uint64_t)d * 2, (uint64_t)H * d * 2, 64, 1, 64,
-                    true))
+                    true) ||
+      !make_out_tmap(&mO, out, out_dtype == MLA_BF16, d, H, (uint64_t)total_q))
     return MLA_ERR_CUDA;
   FlashArgs fa = {};
   fa.B = B; fa.Tq = max_seqlen_q; fa.Tkv = 0; fa.H = H; fa.R = R; fa.RC = RC; fa.pair = pair;
@@ -455,7 +466,7 @@ mla_status_t mla_latent_attention_varlen(const void* q, const void* kv_latent, c
   fa.cu_q = cu_seqlens_q; fa.cu_kv = cu_seqlens_kv;
   fa.total_q = total_q; fa.total_kv = total_kv;
   return cuda_status(
-      staged(1, stream, [&] { return launch_flash_fused(mQ, mL, mWk, mWv, fa, stream); }));
+      staged(1, stream, [&] { return launch_flash_fused(mQ, mL, mWk, mWv, mO, fa, stream); }));
 }
 
 mla_status_t mla_explicit_attention(const void* q, const void* k, const void* v, void* out, int B,
