@@ -39,6 +39,7 @@
 // columns); warp 14 forwards receive-buffer releases to the peer (CTA pair
 // only).  Warp w reads TMEM lanes 32*(w%4)..+31.
 #include <cuda_bf16.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "internal.h"
@@ -71,19 +72,18 @@ static_assert(kSmemBytes <= 232448, "dynamic shared memory limit");
 // Fused prefill staging (d <= 128, RC <= 256).  Prologue: the q tile (d/64 x
 // 16 KB) in the P buffers and this CTA's w_up_k rows (d/64 x RC*128 B) in the
 // receive buffers, both free until q' is in TMEM, so the latent ring starts at
-// once.  Epilogue, inside the latent ring: w_up_v rows (d/64 x RC*128 B) in the
-// stages that tiles nt and nt+1 would take (free as soon as P.L of tiles nt-4
-// and nt-3 has completed, so the load overlaps the end of the loop) and the
-// normalised O_lat (bf16, RC/64 x 16 KB) in the stages of tiles nt-2 and nt-1.
+// once.  Epilogue: w_up_v rows (d/64 x RC*128 B) in the ring stages that tiles
+// nt and nt+1 would take (free as soon as P.L of tiles nt-4 and nt-3 has
+// completed, so the load overlaps the end of the loop); the normalised O_lat
+// goes to TMEM as bf16 (q''s columns) and the output tile, once computed, is
+// staged for its tile store at the start of the ring.
 static_assert(2 * kRows * 128 <= 2 * kPBytes, "q tile staging");
 static_assert(2 * kMaxRC * 128 <= kXBuf * kXBytes, "w_up_k staging");
-static_assert(kMaxRC * 128 <= kLStage && 2 * kRows * 128 <= kLStage, "epilogue staging");
+static_assert(kMaxRC * 128 <= kLStage, "w_up_v staging");
 
 struct EpiStages {
   uint32_t wv_lo;    // stage of w_up_v chunk 0 (d columns 0..63)
   uint32_t wv_lbo;   // byte distance to chunk 1 (d columns 64..127)
-  uint32_t o_a;      // stage of O_lat chunks 0, 1 (rank columns 0..127)
-  uint32_t o_b;      // stage of O_lat chunks 2, 3
 };
 
 __device__ __forceinline__ EpiStages epi_stages(int nt, int dch) {
@@ -91,14 +91,7 @@ __device__ __forceinline__ EpiStages epi_stages(int nt, int dch) {
   EpiStages e;
   e.wv_lo = dch > 1 ? min(s0, s1) : s0;
   e.wv_lbo = dch > 1 ? (max(s0, s1) - min(s0, s1)) * (uint32_t)kLStage : (uint32_t)kLStage;
-  e.o_a = (uint32_t)((nt + 2) % kStages);
-  e.o_b = (uint32_t)((nt + 3) % kStages);
   return e;
-}
-
-// Shared-memory byte offset of 16 KB O_lat chunk c (64 rank columns x 128 rows).
-__device__ __forceinline__ uint32_t epi_o_chunk(const EpiStages& e, uint32_t c) {
-  return (c < 2 ? e.o_a : e.o_b) * (uint32_t)kLStage + (c & 1u) * (uint32_t)(kRows * 128);
 }
 
 constexpr uint32_t kTmemO = 0;       // columns [0, RC)
@@ -129,6 +122,23 @@ struct Bars {
 };
 
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
+
+// The barriers are initialised one per lane of warp 0: their index in the
+// block above and the arrival count each expects.
+constexpr int kNumBars = 37;
+static_assert(offsetof(Bars, q_ready) == 1 * 8 && offsetof(Bars, s_empty) == 12 * 8 &&
+                  offsetof(Bars, p_full) == 14 * 8 && offsetof(Bars, o_last) == 18 * 8 &&
+                  offsetof(Bars, x_consumed) == 27 * 8 && offsetof(Bars, epi_a) == 33 * 8 &&
+                  offsetof(Bars, epi_x) == (kNumBars - 1) * 8,
+              "barrier indices");
+
+__device__ __forceinline__ uint32_t bar_arrivals(int i, bool pair) {
+  if (i == 1 || i == 14 || i == 15 || i == 33) return 256;   // q_ready, p_full, epi_a
+  if (i == 12 || i == 13) return pair ? 384 : 256;           // s_empty (+ exchange warps)
+  if (i == 18) return 2;                                     // o_last: one per MMA issuer
+  if (i >= 27 && i <= 30) return 8;                          // x_consumed: softmax warps
+  return 1;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -252,33 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int nchunk = RC / 64;
   constexpr uint32_t kVOff = kKeys * kRC * 2;   // explicit mode: V tile after the K tile
 
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_ready, 256);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->l_full[s], 1);
-      mbar_init(&bars->l_empty[s], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], a.pair ? 384 : 256);
-      mbar_init(&bars->p_full[i], 256);
-      mbar_init(&bars->p_empty[i], 1);
-    }
-    for (int i = 0; i < kXBuf; ++i) {
-      mbar_init(&bars->x_full[i], 1);      // armed by one local thread; bytes from the peer
-      mbar_init(&bars->x_empty[i], 1);     // forwarded by the peer's forwarding warp
-      mbar_init(&bars->x_consumed[i], 8);  // one arrival per local softmax warp
-    }
-    mbar_init(&bars->o_last, 2);          // one commit per MMA issuer
-    mbar_init(&bars->pro_full, 1);
-    mbar_init(&bars->pro_done, 1);
-    mbar_init(&bars->epi_a, 256);
-    mbar_init(&bars->epi_w, 1);
-    mbar_init(&bars->epi_done, 1);
-    mbar_init(&bars->epi_x, 1);
-    bars->abort_flag = 0;
-    fence_mbarrier_init_cluster();
+  if (warp == 0) {
+    uint64_t* const bar0 = &bars->q_full;
+    for (int i = lane; i < kNumBars; i += 32) mbar_init(bar0 + i, bar_arrivals(i, a.pair != 0));
+    if (lane == 0) bars->abort_flag = 0;
+    fence_mbarrier_init_cluster();   // every lane: its own inits
   }
   if (warp == 1) tmem_alloc(&bars->tmem_slot, 512);
   tc_fence_before();
@@ -478,10 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bv = make_sdesc_sw128(l0 + es.wv_lo * kLStage, es.wv_lbo, 1024);
 #pragma unroll
             for (int k = 0; k < kRC / 16; ++k)
-              umma_bf16(tmem + kTmemS,
-                        make_sdesc_sw128(l0 + epi_o_chunk(es, (uint32_t)(k >> 2)) + (k & 3) * 32,
-                                         16, 1024),
-                        bv + (uint64_t)((k * 2048) >> 4), idesc_v, k > 0 ? 1u : 0u);
+              umma_bf16_ta(tmem + kTmemS, tq + k * 8, bv + (uint64_t)((k * 2048) >> 4), idesc_v,
+                           k > 0 ? 1u : 0u);
           }
           umma_commit(&bars->epi_done);
         }
@@ -749,10 +735,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     if constexpr (kFused) {
-      // normalised O_lat (bf16) -> shared memory, the A operand of the output MMA
+      // normalised O_lat as bf16 pairs in q''s columns (free once the last S
+      // has been computed): the A operand of the output MMA, from TMEM
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      const uint32_t a0s = smem_u32(sL);
-      const EpiStages es = epi_stages(nt, a.d / 64);
       for (int c = oc0; c < oc0 + RC / 2; c += 32) {
         float o[32];
         if (have_o) {
@@ -762,16 +747,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0.f;
         }
-        const uint32_t base = a0s + epi_o_chunk(es, (uint32_t)(c >> 6));
+        float pk[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_shared_v4(base + sw128_offset((uint32_t)r, (uint32_t)(((c & 63) >> 3) + q)),
-                       pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
-                       pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                       pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                       pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+        for (int e = 0; e < 16; ++e)
+          pk[e] = __uint_as_float(pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv));
+        tmem_st16(tmem + lane_base + kTmemQ + c / 2, pk);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->epi_a);
       // out[b, i, h, :] = O_lat . w_up_v[:, h, :]; a CTA pair adds the peer's
