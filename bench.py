@@ -247,7 +247,6 @@ def run_ours(args, rank: int, world: int):
         step()
     torch.cuda.synchronize()
 
-    ev = [mla.StageEvents() for _ in range(args.steps)]
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -260,16 +259,26 @@ def run_ours(args, rank: int, world: int):
     launches0 = mla.launch_count()
     for k in range(args.steps):
         flush.zero_()                          # L2 flush between timed steps (outside the events)
-        ev[k].install()
         starts[k].record(stream)
         step()
         ends[k].record(stream)
     torch.cuda.synchronize()
-    mla.StageEvents.uninstall()
     launches = mla.launch_count() - launches0
-    clocks = sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
+    # The same loop again with the library's per-kernel events (caller events
+    # recorded around each kernel on the launching stream): the kernels'
+    # own durations for the roofline.  Events between kernels end the overlap
+    # of a kernel's set-up with its predecessor's tail, so the step time above
+    # is taken without them.
+    ev = [mla.StageEvents() for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k].install()
+        step()
+    torch.cuda.synchronize()
+    mla.StageEvents.uninstall()
+    clocks = sampler.stop()
     flash_ms = [e.elapsed_ms(1) for e in ev]
     stage_ids = [(4, "projection"), (1, "attention_fused")] if fused else \
         [(4, "projection"), (0, "absorb"), (1, "flash"), (3, "v_up")]
@@ -384,19 +393,23 @@ def run_ours(args, rank: int, world: int):
         for _ in range(max(3, args.warmup)):
             xstep()
         n = max(5, min(args.steps, 20))
-        xev = [mla.StageEvents() for _ in range(n)]
         xs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         xe = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         torch.cuda.synchronize()
         for k_i in range(n):
             flush.zero_()
-            xev[k_i].install()
             xs[k_i].record(stream)
             xstep()
             xe[k_i].record(stream)
         torch.cuda.synchronize()
-        mla.StageEvents.uninstall()
         xms = statistics.mean(a.elapsed_time(b) for a, b in zip(xs, xe))
+        xev = [mla.StageEvents() for _ in range(n)]          # per-kernel times: a second loop
+        for k_i in range(n):
+            flush.zero_()
+            xev[k_i].install()
+            xstep()
+        torch.cuda.synchronize()
+        mla.StageEvents.uninstall()
         xattn = statistics.mean(e.elapsed_ms(1) for e in xev)
         xflops_attn = 4 * w.d * w.pairs() * w.H            # q.k and p.v over d
         expl = {"workload": "prefill_bf16, k and v materialised (bf16) by the projection, then "
@@ -455,7 +468,8 @@ def run_ours(args, rank: int, world: int):
 def time_attention_only(w, dev, flush, stream, n: int, warmup: int):
     """Mean CUDA-event time (ms) of one attention call on workload w with its
     inputs resident and the L2 flushed before every call (outside the events),
-    and the mean time of its main attention kernel (library stage events)."""
+    and, from a second loop with the library's per-kernel events, the mean
+    time of its main attention kernel."""
     import torch
 
     import latent_causal_attention_gb300 as mla
@@ -472,19 +486,23 @@ def time_attention_only(w, dev, flush, stream, n: int, warmup: int):
 
     for _ in range(warmup):
         call()
-    evs = [mla.StageEvents() for _ in range(n)]
     s_ = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     e_ = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     torch.cuda.synchronize()
     for k in range(n):
         flush.zero_()
-        evs[k].install()
         s_[k].record(stream)
         call()
         e_[k].record(stream)
     torch.cuda.synchronize()
-    mla.StageEvents.uninstall()
     ms = statistics.mean(a.elapsed_time(b) for a, b in zip(s_, e_))
+    evs = [mla.StageEvents() for _ in range(n)]
+    for k in range(n):
+        flush.zero_()
+        evs[k].install()
+        call()
+    torch.cuda.synchronize()
+    mla.StageEvents.uninstall()
     kernel_ms = statistics.mean(e.elapsed_ms(1) for e in evs)
     return ms, kernel_ms
 

@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kExplicit = kMode == kModeExplicit;
   constexpr bool kPerHead = kMode != kModePacked;     // rows = query positions of one head
   static_assert(!kExplicit || kRC <= 128, "K and V tiles share one 32 KB stage");
+  grid_dep_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int csize = a.pair ? 2 : 1;
   const uint32_t crank = a.pair ? cluster_ctarank() : 0u;
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int q0 = b * a.Tq, kv0 = b * a.Tkv, Tq_b = a.Tq, Tkv_b = a.Tkv;
   const bool varlen = kPerHead && a.cu_q != nullptr;
   if (varlen) {
+    grid_dep_wait();                       // the offsets may come from the previous kernel
     q0 = a.cu_q[b];
     Tq_b = a.cu_q[b + 1] - q0;
     kv0 = a.cu_kv[b];
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (a.pair) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
+  grid_dep_wait();        // set-up above overlaps the previous kernel's tail
 
   if (warp == 0) {
     // ======================= TMA producer =======================
@@ -1015,13 +1018,15 @@ static cudaError_t launch_flash_rc(const CUtensorMap& mapQ, const CUtensorMap& m
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, mapO, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

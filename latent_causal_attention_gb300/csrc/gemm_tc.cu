@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  grid_dep_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BN = g.BN;
   const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kBM, grp = blockIdx.z;
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();        // set-up above overlaps the previous kernel's tail
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -184,7 +186,18 @@ static cudaError_t launch_shape(const CUtensorMap& mapA, const CUtensorMap& mapB
   constexpr int smem = GemmShape<kWide>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, smem, stream>>>(mapA, mapB, args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k, mapA, mapB, args);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -337,6 +337,19 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Programmatic dependent launch.  grid_dep_wait: block until the grids this
+// one was launched behind have completed and their memory operations are
+// visible (immediate for a grid launched without the attribute).
+// grid_dep_trigger: let the grid launched behind this one be scheduled once
+// every CTA of this grid has triggered or exited; it still waits for this
+// grid's completion before touching memory.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier `id` (1..15) over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
