@@ -407,3 +407,58 @@ def test_two_streams_run_independent_calls(oracle):
         for o, r in zip(outs, refs):
             assert torch.equal(o, r)
     assert mla.device_error() == 0
+
+
+def test_stream_order_with_neighbouring_kernels():
+    """The library's kernels start their set-up while the previous kernel on the
+    stream finishes (programmatic dependent launch) and touch global memory only
+    after it completes.  Torch kernels rewrite the inputs in place right before
+    each call and copy, then poison, the output right after it; every copy must
+    equal the result of a call made in isolation, and no write may land after
+    the poison."""
+    shapes = [custom_workload("dec", dtype="bf16", B=2, Tq=1, Tkv=700, H=16, d=64, rank=512),
+              custom_workload("pre", dtype="bf16", B=1, Tq=256, Tkv=256, H=4, d=128, rank=512),
+              custom_workload("mid", dtype="bf16", B=2, Tq=192, Tkv=192, H=2, d=64, rank=256)]
+    for w in shapes:
+        xs = [{k: cuda(v) for k, v in make_inputs(w, seed=90 + s).items()} for s in range(2)]
+        refs = []
+        for x in xs:
+            refs.append(mla.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale))
+            torch.cuda.synchronize()
+        q, lat = torch.empty_like(xs[0]["q"]), torch.empty_like(xs[0]["kv_latent"])
+        out = torch.empty_like(refs[0])
+        ws = torch.empty(max(1, mla.workspace_size(w.B, w.Tq, w.Tkv, w.H, w.d, w.rank,
+                                                   torch.bfloat16)),
+                         device="cuda", dtype=torch.uint8)
+        snaps = []
+        for i in range(6):
+            x = xs[i % 2]
+            q.copy_(x["q"])
+            lat.copy_(x["kv_latent"])
+            mla.attention(q, lat, x["w_up_k"], x["w_up_v"], w.scale, out=out, workspace=ws)
+            snaps.append(out.clone())
+            out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        for i, snap in enumerate(snaps):
+            assert torch.equal(snap, refs[i % 2]), (w.name, i)
+        assert torch.isnan(out).all(), w.name
+    # the projection's latent consumed by the attention on the same stream
+    w = custom_workload("chain", dtype="bf16", B=1, Tq=256, Tkv=256, H=4, d=64, rank=256)
+    x = {k: cuda(v) for k, v in make_inputs(w, seed=95).items()}
+    hidden = torch.randn(w.B, w.Tkv, 512, generator=torch.Generator().manual_seed(96)
+                         ).to(torch.bfloat16).cuda()
+    w_down = (torch.randn(512, w.rank, generator=torch.Generator().manual_seed(97)) / 22.6
+              ).to(torch.bfloat16).cuda()
+    lat_ref = mla.project(hidden, w_down)[0]
+    ref = mla.attention(x["q"], lat_ref, x["w_up_k"], x["w_up_v"], w.scale)
+    torch.cuda.synchronize()
+    lat = torch.empty_like(lat_ref)
+    for _ in range(4):
+        lat.fill_(float("nan"))
+        mla.project(hidden, w_down, latent=lat)
+        out = mla.attention(x["q"], lat, x["w_up_k"], x["w_up_v"], w.scale)
+        got = out.clone()
+        lat.fill_(float("nan"))
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+    assert mla.device_error() == 0
