@@ -273,7 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(&bars->tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
-  if (a.pair) cluster_sync();
+  // CTA pair: every thread announces that this CTA's barriers exist; only the
+  // warps that touch the peer's shared memory (exchange, release forwarding)
+  // wait for the peer's announcement before their loops, the others just
+  // before the exit barrier, so the round trip is off the prologue's path.
+  const bool touches_peer = (warp >= 2 && warp < 6) || warp == 14;
+  if (a.pair) cluster_arrive();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
   grid_dep_wait();        // set-up above overlaps the previous kernel's tail
@@ -478,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 6) {
     // ======================= partial-S exchange (CTA pair) =======================
+    if (a.pair) cluster_wait();
     if (a.pair && nt > 0) {
       const int qd = warp & 3;
       const uint32_t r = (uint32_t)(qd * 32 + lane);
@@ -537,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // peer's x_empty[b]: the initial release of every buffer, then one per tile.
     // The cluster-scope arrival is a round trip; keeping it on this warp keeps
     // it off the softmax warps' path.
+    if (a.pair) cluster_wait();
     if (a.pair && nt > 0 && lane == 0) {
       const uint32_t xe_peer0 = mapa_shared(smem_u32(&bars->x_empty[0]), peer);
       for (int n = 0; n < nt + kXBuf; ++n) {
@@ -928,7 +935,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 512);
-  if (a.pair) cluster_sync();
+  if (a.pair) {
+    if (!touches_peer) cluster_wait();
+    cluster_sync();     // neither CTA leaves while the other may still address it
+  }
 }
 
 // ---------------------------------------------------------------------------
