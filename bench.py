@@ -298,7 +298,7 @@ def run_ours(args, rank: int, world: int):
     host_out = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = host_out[0].numel() * host_out[0].element_size()
-    e2e_steps = max(3, min(args.steps, 10))
+    e2e_steps = max(3, args.steps)
     dbuf = [d, {k_: torch.empty_like(v_) for k_, v_ in d.items()}]
     obuf = [out, torch.empty_like(out)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)

@@ -40,7 +40,8 @@ struct GemmShape {
 template <bool kBMN, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
-                   const __grid_constant__ CUtensorMap mapB, GemmArgs g) {
+                   const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapC, int c_tile_store, GemmArgs g) {
   constexpr int kStages = GemmShape<kWide>::kStages;
   constexpr int kBStage = GemmShape<kWide>::kBStage;
   constexpr int kTmemCols = GemmShape<kWide>::kTmemCols;
@@ -131,35 +132,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
 
   // ---------------- epilogue: TMEM -> registers -> global ----------------
+  // With c_tile_store the 128 x BN tile is staged in the (now idle) operand
+  // stages as 128-byte-swizzled boxes of 128 rows x 128 bytes and leaves by TMA
+  // tile stores (rows past M are clipped by the map); otherwise each thread
+  // writes its own row.
   const bool ok = mbar_wait(accum, 0, 3, abort_flag);
   __syncwarp();
   tc_fence_after();
+  const uint32_t stage0 = smem_u32(smem);
   if (ok) {
-    const int row = m0 + warp * 32 + lane;
+    const int r = warp * 32 + lane;
+    const int row = m0 + r;
     const bool valid = row < g.M;
     const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      tmem_ld32(tbase + c * 32, v);
+    // two 32-column loads in flight per wait (BN is a multiple of 64)
+    for (int c2 = 0; c2 < BN / 32; c2 += 2) {
+      float vv[2][32];
+      tmem_ld32(tbase + c2 * 32, vv[0]);
+      tmem_ld32(tbase + c2 * 32 + 32, vv[1]);
       tmem_wait_ld();
-      if (valid) {
-        const int64_t off = (int64_t)grp * g.c_gs + (int64_t)row * g.c_rs + n0 + c * 32;
-        if (g.c_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g.C) + off);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(pack_bf16x2(v[8 * q] * g.alpha, v[8 * q + 1] * g.alpha),
-                                pack_bf16x2(v[8 * q + 2] * g.alpha, v[8 * q + 3] * g.alpha),
-                                pack_bf16x2(v[8 * q + 4] * g.alpha, v[8 * q + 5] * g.alpha),
-                                pack_bf16x2(v[8 * q + 6] * g.alpha, v[8 * q + 7] * g.alpha));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(g.C) + off);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int c = c2 + h2;
+        const float (&v)[32] = vv[h2];
+        if (c_tile_store) {
+          if (g.c_bf16) {           // 32 columns = half a box row
+            const uint32_t box = stage0 + (uint32_t)(c >> 1) * (kBM * 128);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(v[4 * q] * g.alpha, v[4 * q + 1] * g.alpha,
-                                 v[4 * q + 2] * g.alpha, v[4 * q + 3] * g.alpha);
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(box + sw128_offset((uint32_t)r, (uint32_t)((c & 1) * 4 + q)),
+                           pack_bf16x2(v[8 * q] * g.alpha, v[8 * q + 1] * g.alpha),
+                           pack_bf16x2(v[8 * q + 2] * g.alpha, v[8 * q + 3] * g.alpha),
+                           pack_bf16x2(v[8 * q + 4] * g.alpha, v[8 * q + 5] * g.alpha),
+                           pack_bf16x2(v[8 * q + 6] * g.alpha, v[8 * q + 7] * g.alpha));
+          } else {                  // 32 columns = one box row
+            const uint32_t box = stage0 + (uint32_t)c * (kBM * 128);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_shared_v4(box + sw128_offset((uint32_t)r, (uint32_t)q),
+                           __float_as_uint(v[4 * q] * g.alpha),
+                           __float_as_uint(v[4 * q + 1] * g.alpha),
+                           __float_as_uint(v[4 * q + 2] * g.alpha),
+                           __float_as_uint(v[4 * q + 3] * g.alpha));
+          }
+        } else if (valid) {
+          const int64_t off = (int64_t)grp * g.c_gs + (int64_t)row * g.c_rs + n0 + c * 32;
+          if (g.c_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g.C) + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16x2(v[8 * q] * g.alpha, v[8 * q + 1] * g.alpha),
+                                  pack_bf16x2(v[8 * q + 2] * g.alpha, v[8 * q + 3] * g.alpha),
+                                  pack_bf16x2(v[8 * q + 4] * g.alpha, v[8 * q + 5] * g.alpha),
+                                  pack_bf16x2(v[8 * q + 6] * g.alpha, v[8 * q + 7] * g.alpha));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(g.C) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(v[4 * q] * g.alpha, v[4 * q + 1] * g.alpha,
+                                   v[4 * q + 2] * g.alpha, v[4 * q + 3] * g.alpha);
+          }
         }
       }
+    }
+  }
+  if (c_tile_store) {
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (ok && threadIdx.x == 0) {
+      const int box_cols = g.c_bf16 ? 64 : 32;
+      for (int bx = 0; bx < BN / box_cols; ++bx)
+        tma_store_3d(&mapC, stage0 + (uint32_t)bx * (kBM * 128), n0 + bx * box_cols, m0, grp);
+      bulk_commit_group();
+      bulk_wait_read_all();
     }
   }
   tc_fence_before();
@@ -186,6 +231,25 @@ static cudaError_t launch_shape(const CUtensorMap& mapA, const CUtensorMap& mapB
   constexpr int smem = GemmShape<kWide>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // The output tile store: C as {N, M, G} with 128-byte boxes of 128 rows,
+  // when the tile fits the operand stages and C's layout suits TMA; else the
+  // kernel writes row by row.
+  const int es = args.c_bf16 ? 2 : 4;
+  const int64_t gs = args.G > 1 ? args.c_gs : (int64_t)args.M * args.c_rs;
+  CUtensorMap mapC;
+  constexpr int64_t kStageBytes =
+      (int64_t)GemmShape<kWide>::kStages * (kAStage + GemmShape<kWide>::kBStage);
+  int tile_store =
+      (int64_t)kBM * args.BN * es <= kStageBytes &&
+      (reinterpret_cast<uintptr_t>(args.C) & 15) == 0 && (args.c_rs * es) % 16 == 0 &&
+      (gs * es) % 16 == 0 && (args.BN * es) % 128 == 0 && (args.N * es) % 16 == 0;
+  if (tile_store)
+    tile_store = make_tmap_3d(&mapC, args.C, es, (uint64_t)args.N, (uint64_t)args.M,
+                              (uint64_t)args.G, (uint64_t)args.c_rs * es, (uint64_t)gs * es,
+                              128u / es, kBM, 1, true)
+                     ? 1
+                     : 0;
+  if (!tile_store) mapC = mapA;                 // not read
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -196,7 +260,7 @@ static cudaError_t launch_shape(const CUtensorMap& mapA, const CUtensorMap& mapB
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k, mapA, mapB, args);
+  e = cudaLaunchKernelEx(&cfg, k, mapA, mapB, mapC, tile_store, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
