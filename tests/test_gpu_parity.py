@@ -462,3 +462,57 @@ def test_stream_order_with_neighbouring_kernels():
         torch.cuda.synchronize()
         assert torch.equal(got, ref)
     assert mla.device_error() == 0
+
+
+def test_calls_capture_into_a_cuda_graph():
+    """The calls make no host synchronisation or allocation of their own, so
+    they can be captured into a CUDA graph (the programmatic launches become
+    programmatic graph edges); replays equal eager calls bit for bit."""
+    cases = [custom_workload("dec", dtype="bf16", B=4, Tq=1, Tkv=900, H=32, d=64, rank=512),
+             custom_workload("pre", dtype="bf16", B=1, Tq=384, Tkv=384, H=4, d=128, rank=512)]
+    for w in cases:
+        x = {k: cuda(v) for k, v in make_inputs(w, seed=110).items()}
+        out = torch.empty(w.B, w.Tq, w.H, w.d, device="cuda", dtype=torch.float32)
+        ws = torch.empty(max(1, mla.workspace_size(w.B, w.Tq, w.Tkv, w.H, w.d, w.rank,
+                                                   torch.bfloat16)),
+                         device="cuda", dtype=torch.uint8)
+        eager = mla.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):          # warm-up on the capture stream
+            mla.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale, out=out,
+                          workspace=ws)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            mla.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale, out=out,
+                          workspace=ws)
+        for _ in range(3):
+            out.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out, eager), w.name
+    # projection + attention in one graph
+    w = custom_workload("chain", dtype="bf16", B=1, Tq=256, Tkv=256, H=4, d=64, rank=256)
+    x = {k: cuda(v) for k, v in make_inputs(w, seed=111).items()}
+    hidden = torch.randn(w.B, w.Tkv, 512, generator=torch.Generator().manual_seed(112)
+                         ).to(torch.bfloat16).cuda()
+    w_down = (torch.randn(512, w.rank, generator=torch.Generator().manual_seed(113)) / 22.6
+              ).to(torch.bfloat16).cuda()
+    lat = torch.empty(w.B, w.Tkv, w.rank, device="cuda", dtype=torch.bfloat16)
+    out = torch.empty(w.B, w.Tq, w.H, w.d, device="cuda", dtype=torch.float32)
+    mla.project(hidden, w_down, latent=lat)
+    eager = mla.attention(x["q"], lat, x["w_up_k"], x["w_up_v"], w.scale)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        mla.project(hidden, w_down, latent=lat)
+        mla.attention(x["q"], lat, x["w_up_k"], x["w_up_v"], w.scale, out=out)
+    for _ in range(3):
+        lat.fill_(float("nan"))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert mla.device_error() == 0
