@@ -55,7 +55,7 @@ constexpr int kStages = 4;           // latent tile ring
 constexpr int kXBuf = 4;             // receive buffers of partial S (CTA pair)
 constexpr int kMaxRC = 256;          // rank columns per CTA
 constexpr int kThreads = 512;          // 16 warps
-constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
 
 constexpr int kLStage = kKeys * kMaxRC * 2;       // 32 KB
 constexpr int kPBytes = kRows * kKeys * 2;        // 16 KB
@@ -188,6 +188,36 @@ __device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) a[c] = a[c] + a[c + 4];
   return (a[0] + a[2]) + (a[1] + a[3]);
+}
+
+// This thread's row of fp32 TMEM columns [src, src+n) times s, as bf16 pairs at
+// columns [dst, dst+n/2) (n a multiple of 32; two 32-column loads per wait).
+__device__ __forceinline__ void tmem_rows_to_bf16(uint32_t src, uint32_t dst, int n, float s) {
+  int c = 0;
+  for (; c + 64 <= n; c += 64) {
+    float v[2][32];
+    tmem_ld32(src + c, v[0]);
+    tmem_ld32(src + c + 32, v[1]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        pk[e] = __uint_as_float(pack_bf16x2(v[h][2 * e] * s, v[h][2 * e + 1] * s));
+      tmem_st16(dst + (c + 32 * h) / 2, pk);
+    }
+  }
+  if (c < n) {
+    float v[32];
+    tmem_ld32(src + c, v);
+    tmem_wait_ld();
+    float pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      pk[e] = __uint_as_float(pack_bf16x2(v[2 * e] * s, v[2 * e + 1] * s));
+    tmem_st16(dst + c / 2, pk);
+  }
 }
 
 // Kernel modes: head-packed rows with q' from the workspace; the fused per-head
@@ -578,16 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(&bars->pro_done, 0, 28, abort_flag);
         if (ok) {
           tc_fence_after();
-          for (int c = oc0; c < oc0 + RC / 2; c += 32) {
-            float v[32];
-            tmem_ld32(tmem + lane_base + kTmemO + c, v);
-            tmem_wait_ld();
-            float pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = __uint_as_float(pack_bf16x2(v[2 * e] * a.qscale, v[2 * e + 1] * a.qscale));
-            tmem_st16(tmem + lane_base + kTmemQ + c / 2, pk);
-          }
+          tmem_rows_to_bf16(tmem + lane_base + kTmemO + oc0, tmem + lane_base + kTmemQ + oc0 / 2,
+                            RC / 2, a.qscale);
           if (a.pair && warp == 6 && lane == 0)
             mbar_arrive_expect_tx(&bars->epi_x, (uint32_t)(kRows * (a.d / 2) * 4));
         }
@@ -748,20 +770,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // normalised O_lat as bf16 pairs in q''s columns (free once the last S
       // has been computed): the A operand of the output MMA, from TMEM
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      for (int c = oc0; c < oc0 + RC / 2; c += 32) {
-        float o[32];
-        if (have_o) {
-          tmem_ld32(tmem + lane_base + kTmemO + c, o);
-          tmem_wait_ld();
-        } else {
+      if (have_o) {
+        tmem_rows_to_bf16(tmem + lane_base + kTmemO + oc0, tmem + lane_base + kTmemQ + oc0 / 2,
+                          RC / 2, inv);
+      } else {
+        float z[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0.f;
-        }
-        float pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = __uint_as_float(pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv));
-        tmem_st16(tmem + lane_base + kTmemQ + c / 2, pk);
+        for (int e = 0; e < 16; ++e) z[e] = 0.f;
+        for (int c = oc0; c < oc0 + RC / 2; c += 32)
+          tmem_st16(tmem + lane_base + kTmemQ + c / 2, z);
       }
       tmem_wait_st();
       tc_fence_before();
