@@ -61,7 +61,7 @@ constexpr int kLStage = kKeys * kMaxRC * 2;       // 32 KB
 constexpr int kPBytes = kRows * kKeys * 2;        // 16 KB
 constexpr int kXBytes = kRows * kKeys * 2;        // 16 KB per receive buffer (fp16 partial S)
 constexpr int kOffL = 0;
-constexpr int kOffP = kOffL + kStages * kLStage;  // P and receive buffers: staging of q' (64 KB)
+constexpr int kOffP = kOffL + kStages * kLStage;  // P, then receive buffers (prologue staging)
 constexpr int kOffX = kOffP + 2 * kPBytes;
 constexpr int kOffRed = kOffX + kXBuf * kXBytes;  // 2 x 128 floats: softmax warp-pair exchange
 constexpr int kOffBar = kOffRed + 1024;
