@@ -213,6 +213,20 @@ def test_projection_bf16_with_kv(oracle):
     assert_bf16_close(v.float(), rv, "v")
 
 
+@pytest.mark.parametrize("R", [64, 256])
+def test_projection_bf16_in_fp32_latent(oracle, R):
+    """bf16 inputs, fp32 latent (tensor-core GEMM, fp32 output tiles; 200 rows:
+    a full and a ragged 128-row tile): fp32 accumulation against float64."""
+    g = torch.Generator().manual_seed(10 + R)
+    M, Dm = 200, 256
+    h = torch.randn(M, Dm, generator=g).bfloat16()
+    wd = (torch.randn(Dm, R, generator=g) / math.sqrt(Dm)).bfloat16()
+    lat, _, _ = mla.project(cuda(h), cuda(wd), out_dtype=torch.float32)
+    rl, _, _ = oracle.project(h, wd)
+    assert lat.dtype == torch.float32
+    assert_f32_close(lat, rl, f"latent fp32 R{R}")
+
+
 # ----------------------------------------------------------------- split-KV merge
 def test_merge_worked_example(oracle):
     """Scores [-inf, 0, 0] as three one-key parts give (v1 + v2) / 2 (page
