@@ -113,7 +113,7 @@ struct Bars {
   uint64_t x_consumed[kXBuf];  // my softmax warps are done with my receive buffer b
   uint64_t pro_full;           // fused prefill: q tile and w_up_k staged (TMA)
   uint64_t pro_done;           // fused prefill: q . w_up_k^T computed into TMEM
-  uint64_t epi_a;              // fused prefill: normalised O_lat (bf16) written to smem
+  uint64_t epi_a;              // fused prefill: normalised O_lat (bf16) written to TMEM
   uint64_t epi_w;              // fused prefill: w_up_v staged (TMA)
   uint64_t epi_done;           // fused prefill: O_lat . w_up_v computed into TMEM
   uint64_t epi_x;              // fused prefill, CTA pair: the peer's partial output arrived
