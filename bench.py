@@ -102,9 +102,15 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
+        return self.summarise(self.lines)
+
+    @classmethod
+    def summarise(cls, lines):
+        """Median SM clock under sampling, the maximum clock and the throttle
+        reasons seen active, from nvidia-smi CSV lines in FIELDS order."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
