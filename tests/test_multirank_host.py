@@ -35,7 +35,7 @@ def _rank(rank, world, port, results):
 
 def test_two_gloo_ranks_take_the_slowest_time_and_count_all_work():
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:     # no fork of a threaded process
         results = mgr.dict()
         mp.spawn(_rank, args=(2, port, results), nprocs=2, join=True)
         got = dict(results)
