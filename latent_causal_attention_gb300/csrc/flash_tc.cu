@@ -81,6 +81,18 @@ static_assert(2 * kRows * 128 <= 2 * kPBytes, "q tile staging");
 static_assert(2 * kMaxRC * 128 <= kXBuf * kXBytes, "w_up_k staging");
 static_assert(kMaxRC * 128 <= kLStage, "w_up_v staging");
 
+// CTA pair, fused epilogue: each CTA sends the peer the half of its partial
+// output that the peer stores, as fp16 rows (128-byte-swizzled, dh/8 16-byte
+// chunks per 128-byte row) multiplied by a power of two that puts the row's
+// largest magnitude in [2^14, 2^15), followed by the inverse factors (one
+// 16-byte slot per row).  The rounding is 2^-11 of the row's largest entry,
+// below the bf16 rounding the normalised O_lat already takes before the output
+// MMA; the scaling keeps any magnitude clear of fp16's range.
+constexpr uint32_t kEpiScaleOff = kRows * 128;
+__device__ __forceinline__ uint32_t epi_x_bytes(int dh) {
+  return (uint32_t)(kRows * (dh * 2 + 16));
+}
+
 struct EpiStages {
   uint32_t wv_lo;    // stage of w_up_v chunk 0 (d columns 0..63)
   uint32_t wv_lbo;   // byte distance to chunk 1 (d columns 64..127)
@@ -555,15 +567,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (okx) {
           tc_fence_after();
           const uint32_t epx_peer = mapa_shared(smem_u32(&bars->epi_x), peer);
-          for (int c = 0; c < dh; c += 16) {
-            float v[16];
-            tmem_ld16(tmem + lane_base + kTmemS + send0 + c, v);
-            tmem_wait_ld();
+          float v[4][16];                               // dh <= 64 columns of my row
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_async_v4(x_peer0 + xrow_offset(r, (uint32_t)((c >> 2) + q), (uint32_t)(dh * 4)),
-                          v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], epx_peer);
-          }
+          for (int c4 = 0; c4 < 4; ++c4)
+            if (c4 * 16 < dh) tmem_ld16(tmem + lane_base + kTmemS + send0 + c4 * 16, v[c4]);
+          tmem_wait_ld();
+          float mx = 0.f;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (c4 * 16 < dh) mx = fmaxf(mx, fabsf(v[c4][e]));
+          // 2^(14 - exponent of mx), as a biased exponent kept inside [1, 253]
+          const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu);
+          const uint32_t sb = (uint32_t)min(max(268 - ex, 1), 253);
+          const float sc = __uint_as_float(sb << 23);
+          const float inv_sc = __uint_as_float((254u - sb) << 23);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              if (c4 * 16 < dh) {
+                const float* w = &v[c4][8 * h];
+                st_async_v4u(x_peer0 + xrow_offset(r, (uint32_t)(2 * c4 + h), 128u),
+                             pack_half2(w[0] * sc, w[1] * sc), pack_half2(w[2] * sc, w[3] * sc),
+                             pack_half2(w[4] * sc, w[5] * sc), pack_half2(w[6] * sc, w[7] * sc),
+                             epx_peer);
+              }
+          st_async_v4u(x_peer0 + kEpiScaleOff + r * 16, __float_as_uint(inv_sc), 0u, 0u, 0u,
+                       epx_peer);
         }
       }
     }
@@ -611,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_rows_to_bf16(tmem + lane_base + kTmemO + oc0, tmem + lane_base + kTmemQ + oc0 / 2,
                             RC / 2, a.qscale);
           if (a.pair && warp == 6 && lane == 0)
-            mbar_arrive_expect_tx(&bars->epi_x, (uint32_t)(kRows * (a.d / 2) * 4));
+            mbar_arrive_expect_tx(&bars->epi_x, epi_x_bytes(a.d / 2));
         }
       } else {
       // q' (staged by TMA in the receive buffers, 128-byte swizzled rows) -> TMEM
@@ -811,16 +843,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (a.pair && have_peer) {
           const int cc = c - (int)crank * dh;          // column within the received half
+          float inv_sc, y0, y1, y2;
+          ld_shared_v4f(x_local + kEpiScaleOff + (uint32_t)r * 16, inv_sc, y0, y1, y2);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float x0, x1, x2, x3;
-            ld_shared_v4f(x_local + xrow_offset((uint32_t)r, (uint32_t)((cc >> 2) + q),
-                                                (uint32_t)(dh * 4)),
-                          x0, x1, x2, x3);
-            v[4 * q] += x0;
-            v[4 * q + 1] += x1;
-            v[4 * q + 2] += x2;
-            v[4 * q + 3] += x3;
+          for (int q = 0; q < 2; ++q) {               // 16 columns = 2 chunks of 8 fp16
+            float x[4];
+            ld_shared_v4f(x_local + xrow_offset((uint32_t)r, (uint32_t)((cc >> 3) + q), 128u),
+                          x[0], x[1], x[2], x[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = unpack_half2(__float_as_uint(x[e]));
+              v[8 * q + 2 * e] += f.x * inv_sc;
+              v[8 * q + 2 * e + 1] += f.y * inv_sc;
+            }
           }
         }
         if (tile_store) {
