@@ -23,7 +23,12 @@
  *     every buffer.  The library never allocates, frees, copies to the host
  *     or synchronises, and never writes its inputs.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
- *     enqueued asynchronously on it.
+ *     enqueued asynchronously on it.  The tensor-core kernels are launched
+ *     with programmatic dependent launch: a kernel may start its own set-up
+ *     (barriers, tensor memory) while the previous kernel on the stream is
+ *     finishing, but reads and writes no global memory before that kernel
+ *     has completed, so stream order is kept.  Calls contain no host
+ *     synchronisation or allocation and can be captured into CUDA graphs.
  *   - The return value reports host-side validation and launch errors only.
  *     A kernel that fails later (for example a device-side wait that ran out
  *     of time, see mla_get_device_error) shows up after the caller's next
