@@ -43,6 +43,22 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _require(name: str, t: Optional[torch.Tensor], shape=None, numel=None, dtype=None,
+             device=None) -> None:
+    """Shape, element count, dtype and device of one argument, checked before
+    any pointer crosses the C ABI (the library trusts the sizes it is given)."""
+    if t is None:
+        return
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+
+
 def _stream(device: torch.device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
@@ -60,12 +76,20 @@ def project(hidden: torch.Tensor, w_down: torch.Tensor, w_up_k: Optional[torch.T
     out_dtype = out_dtype or hidden.dtype
     Dm, R = w_down.shape
     lead = hidden.shape[:-1]
+    if hidden.shape[-1] != Dm:
+        raise ValueError(f"hidden: last dimension {hidden.shape[-1]}, w_down has {Dm} rows")
     M = hidden.numel() // Dm
     kvd = 0
     for w in (w_up_k, w_up_v):
         if w is not None:
             kvd = w.numel() // R
     dev = hidden.device
+    _require("w_down", w_down, dtype=hidden.dtype, device=dev)
+    for name, w in (("w_up_k", w_up_k), ("w_up_v", w_up_v)):
+        _require(name, w, numel=R * kvd, dtype=hidden.dtype, device=dev)
+        if w is not None and (w.shape[0] != R or w.numel() % R != 0):
+            raise ValueError(f"{name}: leading dimension {w.shape[0]}, expected rank {R}")
+    _require("latent", latent, numel=M * R, dtype=out_dtype, device=dev)
     if latent is None:
         latent = torch.empty(*lead, R, device=dev, dtype=out_dtype)
     k = torch.empty(*lead, kvd, device=dev, dtype=out_dtype) if w_up_k is not None else None
@@ -96,6 +120,11 @@ def attention(q: torch.Tensor, kv_latent: torch.Tensor, w_up_k: torch.Tensor,
     B, Tq, H, d = q.shape
     Tkv, R = kv_latent.shape[1], kv_latent.shape[2]
     dev = q.device
+    _require("kv_latent", kv_latent, shape=(B, Tkv, R), dtype=q.dtype, device=dev)
+    _require("w_up_k", w_up_k, numel=R * H * d, dtype=q.dtype, device=dev)
+    _require("w_up_v", w_up_v, numel=R * H * d, dtype=q.dtype, device=dev)
+    _require("out", out, shape=(B, Tq, H, d), device=dev)
+    _require("workspace", workspace, dtype=torch.uint8, device=dev)
     if out is None:
         out = torch.empty(B, Tq, H, d, device=dev, dtype=out_dtype)
     ws_bytes = workspace_size(B, Tq, Tkv, H, d, R, q.dtype, causal)
@@ -121,6 +150,13 @@ def attention_varlen(q: torch.Tensor, kv_latent: torch.Tensor, w_up_k: torch.Ten
     total_q, H, d = q.shape
     total_kv, R = kv_latent.shape
     B = cu_seqlens_q.numel() - 1
+    dev = q.device
+    _require("kv_latent", kv_latent, dtype=q.dtype, device=dev)
+    _require("w_up_k", w_up_k, numel=R * H * d, dtype=q.dtype, device=dev)
+    _require("w_up_v", w_up_v, numel=R * H * d, dtype=q.dtype, device=dev)
+    _require("cu_seqlens_q", cu_seqlens_q, shape=(B + 1,), dtype=torch.int32, device=dev)
+    _require("cu_seqlens_kv", cu_seqlens_kv, shape=(B + 1,), dtype=torch.int32, device=dev)
+    _require("out", out, shape=(total_q, H, d), device=dev)
     if out is None:
         out = torch.empty(total_q, H, d, device=q.device, dtype=out_dtype)
     st = lib.mla_latent_attention_varlen(_ptr(q), _ptr(kv_latent), _ptr(w_up_k), _ptr(w_up_v),
@@ -142,6 +178,9 @@ def explicit_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale:
     lib = _lib.load()
     B, Tq, H, d = q.shape
     Tkv = k.shape[1]
+    _require("k", k, shape=(B, Tkv, H, d), dtype=q.dtype, device=q.device)
+    _require("v", v, shape=(B, Tkv, H, d), dtype=q.dtype, device=q.device)
+    _require("out", out, shape=(B, Tq, H, d), device=q.device)
     if out is None:
         out = torch.empty(B, Tq, H, d, device=q.device, dtype=out_dtype)
     st = lib.mla_explicit_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Tq, Tkv, H, d,
@@ -183,6 +222,9 @@ def merge_partials(m: torch.Tensor, l: torch.Tensor, o: torch.Tensor,
     units, o (parts, rows, width) fp32 -> (rows, width)."""
     lib = _lib.load()
     parts, rows, width = o.shape
+    _require("m", m, shape=(parts, rows), dtype=torch.float32, device=o.device)
+    _require("l", l, shape=(parts, rows), dtype=torch.float32, device=o.device)
+    _require("o", o, dtype=torch.float32)
     out = torch.empty(rows, width, device=o.device, dtype=out_dtype)
     st = lib.mla_merge_partials(_ptr(m), _ptr(l), _ptr(o), _ptr(out), parts, rows, width,
                                 dtype_code(out_dtype), _stream(o.device))
