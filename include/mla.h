@@ -20,7 +20,9 @@
  * Conventions for every call:
  *   - Pointers named as tensors are DEVICE pointers (cudaMalloc'd or from a
  *     framework allocator) to contiguous row-major data; the caller owns
- *     every buffer.  The library never allocates, frees, copies to the host
+ *     every buffer, and each must hold at least the elements its documented
+ *     shape implies (a raw pointer carries no size: the library reads and
+ *     writes exactly those extents and cannot check them).  The library never allocates, frees, copies to the host
  *     or synchronises, and never writes its inputs.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
  *     enqueued asynchronously on it.  The tensor-core kernels are launched
