@@ -53,13 +53,19 @@ def job_throughput(units_per_rank_step: float, steps: int, world: int, max_ms: f
 
 
 def load_peaks():
+    """The roofline denominators: the measured HBM copy and bf16 GEMM rates of
+    this GPU pool when their record is present and complete, else the
+    fallback figures (one earlier GB300 measurement)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             p = json.load(f)
-        return p, "measured"
-    except (OSError, ValueError):
-        return dict(FALLBACK_PEAKS), "fallback"
+        if all(isinstance(p.get(k), (int, float)) and p[k] > 0
+               for k in ("hbm_gbs", "bf16_tflops")):
+            return p, "measured"
+    except (OSError, ValueError, AttributeError):
+        pass
+    return dict(FALLBACK_PEAKS), "fallback"
 
 
 # ------------------------------------------------------------------ clocks

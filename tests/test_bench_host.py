@@ -52,3 +52,17 @@ def test_cpu_baseline_report():
     assert detail["literal_form"]["value"] > 0
     _, plain = bench.time_oracle(budget_s=0.3, seed_rows=6, literal=False)
     assert plain["literal_form"] is None
+
+
+def test_peaks_come_from_the_measured_record_else_the_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    peaks, kind = bench.load_peaks()                       # no record
+    assert kind == "fallback" and peaks["hbm_gbs"] == 6800.0 and peaks["bf16_tflops"] == 1900.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6788.3}))
+    assert bench.load_peaks()[1] == "fallback"             # incomplete record
+    (tmp_path / "MEASURED_PEAKS.json").write_text("not json")
+    assert bench.load_peaks()[1] == "fallback"
+    (tmp_path / "MEASURED_PEAKS.json").write_text(
+        json.dumps({"hbm_gbs": 6788.3, "bf16_tflops": 1909.8, "bf16_tflops_sustained": 1707.2}))
+    peaks, kind = bench.load_peaks()
+    assert kind == "measured" and peaks["bf16_tflops"] == 1909.8
