@@ -257,3 +257,22 @@ def test_explicit_kv_oracle_matches_sdpa():
             tq, tk, tv, attn_mask=mask if causal else None, scale=0.35).permute(0, 2, 1, 3)
         np.testing.assert_allclose(explicit.attention_kv(q, k, v, 0.35, causal), ref.numpy(),
                                    rtol=1e-12, atol=1e-12)
+
+
+def test_projection_flop_count_matches_the_printed_toy_figures():
+    """The FLOP accounting the benchmark uses, on the toy projection workload,
+    against the totals the projection page prints (rounded to 0.1 MFLOP)."""
+    from latent_causal_attention_gb300.inputs import WORKLOADS
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "projection_flops.txt")
+    printed = {}
+    for line in open(path):
+        if line.strip() and not line.startswith("#"):
+            name, val = line.split(":")
+            printed[name.strip()] = float(val)
+    w = WORKLOADS["proj_f32"]
+    assert (w.B * w.Tkv, w.model_dim, w.rank, w.kv_dim) == (384, 256, 48, 128)
+    latent = w.projection_flops(with_kv=False)
+    kv = w.projection_flops(with_kv=True) - latent
+    assert round(latent / 1e6, 1) == printed["latent"]
+    assert round(kv / 2 / 1e6, 1) == printed["k"] == printed["v"]
