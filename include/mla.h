@@ -81,13 +81,19 @@ typedef enum {
  *   w_up_v  (rank, kv_dim)       in_dtype   may be NULL together with v
  *   latent  (M, rank)            out_dtype  written
  *   k, v    (M, kv_dim)          out_dtype  written if non-NULL
- * k and v are computed from the fp32 latent (before any rounding to out_dtype).
- * bf16 inputs use the tensor-core path, which needs 16-byte aligned pointers,
- * model_dim % 64 == 0, rank % 64 == 0 (rank <= 512) and kv_dim % 64 == 0;
- * fp32 inputs take the CUDA-core path (any positive sizes, rank <= 256).
+ * Two paths, chosen from dtype, shape and alignment:
+ *   - tensor-core path: bf16 inputs with 16-byte aligned pointers,
+ *     model_dim % 64 == 0, rank % 64 == 0, rank <= 512 and, when k or v is
+ *     requested, kv_dim % 64 == 0 and out_dtype bf16.  latent is one GEMM
+ *     with fp32 accumulation, rounded once to out_dtype; k and v are then
+ *     computed from that STORED (bf16-rounded) latent, as a caller that
+ *     projects the stored latent itself would get.
+ *   - CUDA-core path (fp32 inputs, or bf16 shapes the tensor-core path does
+ *     not take): any positive sizes with rank <= 512; k and v are computed
+ *     from the fp32 latent held on chip, before it is rounded to out_dtype.
  * Errors: MLA_ERR_NULL (hidden, w_down or latent NULL; k given without
- * w_up_k; v without w_up_v), MLA_ERR_SHAPE, MLA_ERR_DTYPE, MLA_ERR_ALIGN,
- * MLA_ERR_CUDA.
+ * w_up_k; v without w_up_v), MLA_ERR_SHAPE (a non-positive size, M above
+ * 2^31 - 1), MLA_ERR_DTYPE, MLA_ERR_UNSUPPORTED (rank > 512), MLA_ERR_CUDA.
  */
 mla_status_t mla_kv_latent_project(const void* hidden, const void* w_down, const void* w_up_k,
                                    const void* w_up_v, void* latent, void* k, void* v,
@@ -96,10 +102,24 @@ mla_status_t mla_kv_latent_project(const void* hidden, const void* w_down, const
 
 /*
  * Device workspace, in bytes, that mla_latent_attention needs for these sizes
- * (0 when the chosen path needs none).  Pure host function.
+ * (0 when the chosen path needs none).  Host function: it launches nothing;
+ * the first call on a device asks the device for its SM count (see
+ * mla_latent_attention_kv_splits), so make it before any stream capture.
  */
 size_t mla_latent_attention_workspace_size(int B, int Tq, int Tkv, int H, int d, int rank,
                                            int in_dtype, int causal);
+
+/*
+ * Number of key-range partitions mla_latent_attention will use for these
+ * sizes (1 = no split; 0 = the warp-per-query path, which does not split).
+ * When the head-packed tensor-core path has fewer CTAs than half the SMs,
+ * the key range is split so that about one CTA runs per SM.  The SM count
+ * is the current device's (asked once per device and cached), or the value
+ * set with MLA_OPT_NUM_SMS, or 152 when no device can be asked.  Host
+ * function, launches nothing.
+ */
+int mla_latent_attention_kv_splits(int B, int Tq, int Tkv, int H, int d, int rank, int in_dtype,
+                                   int causal);
 
 /*
  * out[b,i,h,:] = sum_s softmax_s(scale * q[b,i,h,:] . k_s) * v_s with
@@ -130,8 +150,11 @@ size_t mla_latent_attention_workspace_size(int B, int Tq, int Tkv, int H, int d,
  *     over the key range when there are few rows), merge and w_up_v GEMM.
  *   - otherwise (fp32, or small/odd shapes): warp-per-query CUDA-core path
  *     (rank <= 1024, d <= 256).
- * Errors: MLA_ERR_NULL, MLA_ERR_SHAPE, MLA_ERR_DTYPE, MLA_ERR_ALIGN,
- * MLA_ERR_WORKSPACE, MLA_ERR_CUDA.
+ * Errors: MLA_ERR_NULL, MLA_ERR_SHAPE (a non-positive size, Tq > Tkv, or
+ * B*Tq*H or B*Tkv above 2^31 - 1), MLA_ERR_DTYPE, MLA_ERR_ALIGN (only with
+ * MLA_OPT_ATTN_PATH forcing the tensor-core path; otherwise misaligned
+ * pointers take the warp path), MLA_ERR_WORKSPACE, MLA_ERR_UNSUPPORTED
+ * (warp path beyond rank 1024 or d 256), MLA_ERR_CUDA.
  */
 mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const void* w_up_k,
                                   const void* w_up_v, void* out, int B, int Tq, int Tkv, int H,
@@ -154,7 +177,10 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
  *
  *   - Returns MLA_ERR_WORKSPACE (nothing launched) when the scratch these
  *     sizes need, mla_latent_attention_workspace_size(...), exceeds
- *     MLA_NOALLOC_SCRATCH_BYTES.  The warp-per-query path needs none.
+ *     MLA_NOALLOC_SCRATCH_BYTES.  The warp-per-query path needs none, so a
+ *     call that mla_latent_attention would send to it (fp32, small or odd
+ *     shapes, or pointers the tensor-core path cannot address) is never
+ *     refused for its size.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.  Later calls only reuse the address.
@@ -260,8 +286,10 @@ mla_status_t mla_check_wait_timeout(unsigned int limit_us, void* stream);
 typedef enum {
   MLA_OPT_ATTN_PATH = 0,       /* 0 auto, 1 force warp path, 2 force tensor-core path */
   MLA_OPT_KV_SPLITS = 1,       /* 0 auto, n > 0 split the key range into n parts      */
-  MLA_OPT_PREFILL_FUSED = 2    /* 1 (default) per-head fused kernel for long prefill,
+  MLA_OPT_PREFILL_FUSED = 2,   /* 1 (default) per-head fused kernel for long prefill,
                                   0 always the head-packed kernels                    */
+  MLA_OPT_NUM_SMS = 3          /* 0 (default) plan for the device's own SM count,
+                                  n > 0 plan for n SMs                                */
 } mla_option_t;
 mla_status_t mla_set_option(int option, int64_t value);
 

@@ -19,7 +19,7 @@ from . import _lib
 from ._lib import MLAError, MLA_BF16, MLA_F32
 
 __all__ = ["project", "attention", "attention_varlen", "explicit_attention", "attention_from_host",
-           "workspace_size",
+           "workspace_size", "kv_splits",
            "merge_partials",
            "set_option", "device_error", "launch_count", "StageEvents", "MLAError",
            "dtype_code"]
@@ -106,6 +106,15 @@ def workspace_size(B: int, Tq: int, Tkv: int, H: int, d: int, rank: int,
     lib = _lib.load()
     return int(lib.mla_latent_attention_workspace_size(B, Tq, Tkv, H, d, rank, dtype_code(dtype),
                                                        int(causal)))
+
+
+def kv_splits(B: int, Tq: int, Tkv: int, H: int, d: int, rank: int,
+              dtype: torch.dtype, causal: bool = True) -> int:
+    """Key-range partitions the attention call plans for these sizes (0: the
+    warp-per-query path)."""
+    lib = _lib.load()
+    return int(lib.mla_latent_attention_kv_splits(B, Tq, Tkv, H, d, rank, dtype_code(dtype),
+                                                  int(causal)))
 
 
 def attention(q: torch.Tensor, kv_latent: torch.Tensor, w_up_k: torch.Tensor,

@@ -12,7 +12,7 @@ MLA_F32, MLA_BF16 = 0, 1
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_NULL", 2: "MLA_ERR_SHAPE", 3: "MLA_ERR_DTYPE",
           4: "MLA_ERR_ALIGN", 5: "MLA_ERR_WORKSPACE", 6: "MLA_ERR_CUDA", 7: "MLA_ERR_TIMEOUT",
           8: "MLA_ERR_UNSUPPORTED"}
-OPT_ATTN_PATH, OPT_KV_SPLITS, OPT_PREFILL_FUSED = 0, 1, 2
+OPT_ATTN_PATH, OPT_KV_SPLITS, OPT_PREFILL_FUSED, OPT_NUM_SMS = 0, 1, 2, 3
 
 _lock = threading.Lock()
 _lib = None
@@ -22,6 +22,7 @@ _vp, _i, _i64, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c
 SIGNATURES = {
     "mla_kv_latent_project": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i, _i, _i, _i, _vp]),
     "mla_latent_attention_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "mla_latent_attention_kv_splits": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "mla_latent_attention": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i,
                                   _vp, _sz, _vp]),
     "mla_latent_attention_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,

@@ -7,7 +7,11 @@
 
 namespace mla {
 
-constexpr int kNumSMsHint = 152;
+// SM count assumed when the device cannot be asked (no GPU visible to the
+// host code that plans a call; a GB300 has 152).
+constexpr int kDefaultNumSMs = 152;
+// Largest row or position count the kernels index with 32-bit integers.
+constexpr int64_t kMaxIndex = ((int64_t)1 << 31) - 1;
 
 // ----- CUDA-core paths ------------------------------------------------------
 cudaError_t launch_warp_attention(const void* q, const void* lat, const void* wk, const void* wv,

@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/mla.h"
@@ -67,6 +68,7 @@ static bool make_out_tmap(CUtensorMap* map, void* out, bool bf16, int d, int H, 
 static int g_attn_path = 0;     // 0 auto, 1 warp, 2 tensor core
 static int g_kv_splits = 0;     // 0 auto
 static int g_prefill_fused = 1; // 1: one fused kernel per head for long prefill
+static int g_num_sms = 0;       // > 0: SM count the planner assumes (0: the device's own)
 static void** g_stage_events = nullptr;
 static int g_stage_events_n = 0;
 static unsigned long long g_launches = 0;
@@ -107,6 +109,29 @@ struct AttnPlan {
   size_t off_qp, off_olat, off_po, off_pml, total;
 };
 
+constexpr int kMaxDevices = 64;
+static std::atomic<int> g_sm_count[kMaxDevices];
+
+// SM count of the current device, asked once per device and cached; the
+// option MLA_OPT_NUM_SMS overrides it, and a host without a usable device
+// plans for kDefaultNumSMs.
+static int planner_sm_count() {
+  if (g_num_sms > 0) return g_num_sms;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();              // leave no error behind for a later launch check
+    return kDefaultNumSMs;
+  }
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return kDefaultNumSMs;
+  }
+  g_sm_count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 static bool tc_shape_ok(int d, int R) {
   if (d % 64 != 0 || d > 256) return false;
   if (R % 64 != 0 || R > 512) return false;
@@ -134,15 +159,16 @@ static AttnPlan plan_attention(int B, int Tq, int Tkv, int H, int d, int R, int 
     p.total = 0;
     return p;
   }
-  p.row_blocks = (int)((int64_t)Tq * H + 127) / 128;
+  p.row_blocks = (int)(((int64_t)Tq * H + 127) / 128);
   const int csize = p.pair ? 2 : 1;
   const int64_t ctas = (int64_t)p.row_blocks * B * csize;
   const int kv_tiles = (Tkv + 63) / 64;
   int splits = 1;
   if (g_kv_splits > 0) {
     splits = g_kv_splits;
-  } else if (ctas < kNumSMsHint / 2) {
-    splits = (int)((kNumSMsHint + ctas - 1) / ctas);
+  } else {
+    const int sms = planner_sm_count();
+    if (ctas < sms / 2) splits = (int)((sms + ctas - 1) / ctas);
   }
   if (splits > kv_tiles) splits = kv_tiles;
   if (splits < 1) splits = 1;
@@ -157,6 +183,12 @@ static AttnPlan plan_attention(int B, int Tq, int Tkv, int H, int d, int R, int 
   }
   p.total = off;
   return p;
+}
+
+// The tensor-core path reads and writes through TMA and 16-byte vectors.
+static bool tc_pointers_ok(const void* q, const void* lat, const void* wk, const void* wv,
+                           const void* out) {
+  return aligned16(q) && aligned16(lat) && aligned16(wk) && aligned16(wv) && aligned16(out);
 }
 
 static mla_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
@@ -195,6 +227,10 @@ mla_status_t mla_set_option(int option, int64_t value) {
     case MLA_OPT_PREFILL_FUSED:
       if (value < 0 || value > 1) return MLA_ERR_SHAPE;
       g_prefill_fused = (int)value;
+      return MLA_OK;
+    case MLA_OPT_NUM_SMS:
+      if (value < 0 || value > 4096) return MLA_ERR_SHAPE;
+      g_num_sms = (int)value;
       return MLA_OK;
     default:
       return MLA_ERR_UNSUPPORTED;
@@ -236,7 +272,7 @@ mla_status_t mla_kv_latent_project(const void* hidden, const void* w_down, const
   if ((k && !w_up_k) || (v && !w_up_v)) return MLA_ERR_NULL;
   if (M <= 0 || model_dim <= 0 || rank <= 0) return MLA_ERR_SHAPE;
   if ((k || v) && kv_dim <= 0) return MLA_ERR_SHAPE;
-  if (M > (int64_t)1 << 31) return MLA_ERR_SHAPE;
+  if (M > kMaxIndex) return MLA_ERR_SHAPE;
   if (in_dtype != MLA_F32 && in_dtype != MLA_BF16) return MLA_ERR_DTYPE;
   if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
   if (in_dtype == MLA_F32 && out_dtype != MLA_F32) return MLA_ERR_DTYPE;
@@ -300,6 +336,13 @@ size_t mla_latent_attention_workspace_size(int B, int Tq, int Tkv, int H, int d,
   return p.tc ? p.total : 0;
 }
 
+int mla_latent_attention_kv_splits(int B, int Tq, int Tkv, int H, int d, int rank, int in_dtype,
+                                   int causal) {
+  if (B <= 0 || Tq <= 0 || Tkv <= 0 || H <= 0 || d <= 0 || rank <= 0 || Tq > Tkv) return 0;
+  AttnPlan p = plan_attention(B, Tq, Tkv, H, d, rank, in_dtype, causal);
+  return p.tc ? p.splits : 0;
+}
+
 mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const void* w_up_k,
                                   const void* w_up_v, void* out, int B, int Tq, int Tkv, int H,
                                   int d, int rank, float scale, int causal, int in_dtype,
@@ -308,16 +351,14 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
   if (!q || !kv_latent || !w_up_k || !w_up_v || !out) return MLA_ERR_NULL;
   if (B <= 0 || Tq <= 0 || Tkv <= 0 || H <= 0 || d <= 0 || rank <= 0 || Tq > Tkv)
     return MLA_ERR_SHAPE;
-  if ((int64_t)B * Tq * H > ((int64_t)1 << 31) || (int64_t)B * Tkv > ((int64_t)1 << 31))
-    return MLA_ERR_SHAPE;
+  if ((int64_t)B * Tq * H > kMaxIndex || (int64_t)B * Tkv > kMaxIndex) return MLA_ERR_SHAPE;
   if (in_dtype != MLA_F32 && in_dtype != MLA_BF16) return MLA_ERR_DTYPE;
   if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
   if (in_dtype == MLA_F32 && out_dtype != MLA_F32) return MLA_ERR_DTYPE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
 
   AttnPlan p = plan_attention(B, Tq, Tkv, H, d, rank, in_dtype, causal);
-  if (p.tc && !(aligned16(q) && aligned16(kv_latent) && aligned16(w_up_k) && aligned16(w_up_v) &&
-                aligned16(out))) {
+  if (p.tc && !tc_pointers_ok(q, kv_latent, w_up_k, w_up_v, out)) {
     if (g_attn_path == 2) return MLA_ERR_ALIGN;
     p.tc = false;
   }
@@ -434,7 +475,7 @@ mla_status_t mla_latent_attention_varlen(const void* q, const void* kv_latent, c
   if (B <= 0 || max_seqlen_q <= 0 || total_q <= 0 || total_kv <= 0 || H <= 0 ||
       max_seqlen_q > total_q)
     return MLA_ERR_SHAPE;
-  if ((int64_t)total_q * H > ((int64_t)1 << 31)) return MLA_ERR_SHAPE;
+  if ((int64_t)total_q * H > kMaxIndex) return MLA_ERR_SHAPE;
   if (d % 64 != 0 || d > 128 || !tc_shape_ok(d, rank)) return MLA_ERR_SHAPE;
   if (in_dtype != MLA_BF16) return MLA_ERR_DTYPE;
   if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
@@ -475,8 +516,7 @@ mla_status_t mla_explicit_attention(const void* q, const void* k, const void* v,
   if (!q || !k || !v || !out) return MLA_ERR_NULL;
   if (B <= 0 || Tq <= 0 || Tkv <= 0 || H <= 0 || Tq > Tkv) return MLA_ERR_SHAPE;
   if (d != 64 && d != 128) return MLA_ERR_SHAPE;
-  if ((int64_t)B * Tq * H > ((int64_t)1 << 31) || (int64_t)B * Tkv * H > ((int64_t)1 << 31))
-    return MLA_ERR_SHAPE;
+  if ((int64_t)B * Tq * H > kMaxIndex || (int64_t)B * Tkv * H > kMaxIndex) return MLA_ERR_SHAPE;
   if (in_dtype != MLA_BF16) return MLA_ERR_DTYPE;
   if (out_dtype != MLA_F32 && out_dtype != MLA_BF16) return MLA_ERR_DTYPE;
   if (!(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out))) return MLA_ERR_ALIGN;
@@ -521,7 +561,6 @@ namespace mla {
 // device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
 static std::mutex g_noalloc_mu;
 static void* g_noalloc_addr[kMaxDevices] = {};
 
@@ -550,8 +589,12 @@ extern "C" mla_status_t mla_latent_attention_noalloc(const void* q, const void* 
                                                      void* out, int B, int Tq, int Tkv, int H,
                                                      int d, int rank, float scale, int causal,
                                                      int in_dtype, int out_dtype, void* stream) {
-  const size_t need =
-      mla_latent_attention_workspace_size(B, Tq, Tkv, H, d, rank, in_dtype, causal);
+  // The scratch the regular call would use: none when it falls back to the
+  // warp path for pointers the tensor-core path cannot address.
+  size_t need = mla_latent_attention_workspace_size(B, Tq, Tkv, H, d, rank, in_dtype, causal);
+  if (need > 0 && mla::g_attn_path != 2 &&
+      !mla::tc_pointers_ok(q, kv_latent, w_up_k, w_up_v, out))
+    need = 0;
   if (need > (size_t)MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0 && mla::noalloc_scratch(&scratch) != cudaSuccess) return MLA_ERR_CUDA;

@@ -152,3 +152,72 @@ def test_product_path_has_no_fallback():
     """Without the built library the binding raises instead of computing."""
     with pytest.raises(RuntimeError):
         _lib.load(path=os.path.join(ROOT, "does_not_exist.so"))
+
+
+def test_planner_follows_the_sm_count(lib):
+    """The key-range split is sized from the SM count the planner is given
+    (MLA_OPT_NUM_SMS), not from a fixed figure: when the head-packed kernels
+    have fewer CTAs than half the SMs, the range is split into about
+    SMs / CTAs parts (capped by the number of 64-key tiles)."""
+    sp = lib.mla_latent_attention_kv_splits
+    # decode, 64 sequences x 128 heads, rank 512: 64 CTA pairs = 128 CTAs
+    dec = (64, 1, 4096, 128, 128, 512, 1, 1)
+    # four sequences: 8 CTAs
+    few = (4, 1, 4096, 128, 128, 512, 1, 1)
+    try:
+        assert lib.mla_set_option(_lib.OPT_NUM_SMS, 152) == 0
+        assert sp(*dec) == 1                       # 128 CTAs >= 76: no split
+        assert sp(*few) == 19                      # ceil(152 / 8)
+        assert lib.mla_set_option(_lib.OPT_NUM_SMS, 512) == 0
+        assert sp(*dec) == 4                       # 128 < 256: ceil(512 / 128)
+        assert sp(*few) == 64                      # ceil(512 / 8), 64 tiles of keys
+        assert sp(4, 1, 1000, 128, 128, 512, 1, 1) == 16   # capped at 16 key tiles
+        assert lib.mla_set_option(_lib.OPT_NUM_SMS, 16) == 0
+        assert sp(*few) == 1                       # 8 CTAs >= 8
+        # the workspace follows the split count (partial O and (m, l) per part)
+        ws16 = lib.mla_latent_attention_workspace_size(*few)
+        assert lib.mla_set_option(_lib.OPT_NUM_SMS, 152) == 0
+        ws152 = lib.mla_latent_attention_workspace_size(*few)
+        assert ws152 >= ws16 + 19 * 4 * 128 * 512 * 4
+        # paths that never split
+        assert sp(2, 4096, 4096, 32, 128, 512, 1, 1) == 1   # fused prefill kernel
+        assert sp(2, 32, 32, 4, 16, 24, 0, 1) == 0          # fp32: warp path
+        assert lib.mla_set_option(_lib.OPT_NUM_SMS, -1) == 2
+    finally:
+        lib.mla_set_option(_lib.OPT_NUM_SMS, 0)
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="host-only: without a device no kernel can start")
+def test_planner_without_a_device_assumes_152_sms(lib):
+    assert lib.mla_latent_attention_kv_splits(4, 1, 4096, 128, 128, 512, 1, 1) == 19
+
+
+def test_row_count_limit_is_exclusive(lib):
+    """B*Tq*H must stay below 2^31 (the kernels index rows with int32):
+    exactly 2^31 rows is refused before anything is planned or launched."""
+    assert attn(lib, B=1, Tq=1 << 30, Tkv=1 << 30, H=2) == 2
+    assert attn(lib, B=2, Tq=8, Tkv=1 << 30, H=1) == 2            # B*Tkv = 2^31
+    # one row fewer passes the shape checks and stops at the missing workspace
+    # of the head-packed kernels (the fused kernel, which needs none, is
+    # switched off so that nothing can be launched)
+    assert lib.mla_set_option(_lib.OPT_PREFILL_FUSED, 0) == 0
+    try:
+        assert attn(lib, B=1, Tq=(1 << 31) - 1, Tkv=(1 << 31) - 1, H=1) == 5
+    finally:
+        lib.mla_set_option(_lib.OPT_PREFILL_FUSED, 1)
+    f = lib.mla_kv_latent_project
+    assert f(P, P, None, None, P, None, None, 1 << 31, 64, 64, 0, 1, 1, None) == 2
+
+
+def test_noalloc_refuses_only_what_its_scratch_cannot_hold(lib):
+    """The allocation-free call refuses sizes whose tensor-core scratch would
+    exceed its fixed array, before launching anything; sizes that need no
+    scratch (fp32, the warp path) are never refused for their size."""
+    big = (8, 32, 4096, 128, 128, 512)              # ~67 MB of head-packed scratch
+    assert lib.mla_latent_attention_workspace_size(*big, 1, 1) > 32 * 1024 * 1024
+    before = lib.mla_launch_count()
+    st = lib.mla_latent_attention_noalloc(P, P, P, P, P, *big, 0.1, 1, 1, 0, None)
+    assert st == 5
+    assert lib.mla_launch_count() == before
+    assert lib.mla_latent_attention_noalloc(None, P, P, P, P, *big, 0.1, 1, 1, 0, None) in (1, 5)
