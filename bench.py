@@ -31,6 +31,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "latent-attention TFLOP/s and HBM GB/s on 1 GB300; fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Published per-GPU figures, reported as a second denominator beside the
+# measured ones: HBM3e bandwidth about 8 TB/s per GB300; dense BF16 tensor
+# throughput 2.25 PFLOP/s per GPU (NVIDIA lists FP16/BF16 tensor throughput of
+# 36 PFLOPS per 8 Blackwell Ultra GPUs of an HGX B300 with 2:4 sparsity; dense
+# is half of the sparse figure).
+SPEC_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0,
+              "source": "NVIDIA Blackwell Ultra (GB300 / HGX B300) specifications: HBM3e 8 TB/s "
+                        "per GPU; FP16/BF16 tensor 36 PFLOPS per 8 GPUs with 2:4 sparsity = "
+                        "2.25 PFLOP/s dense per GPU"}
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -52,16 +61,20 @@ def job_throughput(units_per_rank_step: float, steps: int, world: int, max_ms: f
     return world * units_per_rank_step * steps / (max_ms * 1e-3) / scale
 
 
-def load_peaks():
+def load_peaks(device_name=None):
     """The roofline denominators: the measured HBM copy and bf16 GEMM rates of
-    this GPU pool when their record is present and complete, else the
-    fallback figures (one earlier GB300 measurement)."""
+    this GPU pool when their record is present, complete and taken on the
+    same kind of GPU as ``device_name`` (when given), else the fallback
+    figures (one earlier GB300 measurement)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             p = json.load(f)
         if all(isinstance(p.get(k), (int, float)) and p[k] > 0
                for k in ("hbm_gbs", "bf16_tflops")):
+            rec = p.get("gpu_name")
+            if device_name is not None and rec and rec != device_name:
+                return dict(FALLBACK_PEAKS), f"fallback (the record is for {rec})"
             return p, "measured"
     except (OSError, ValueError, AttributeError):
         pass
@@ -187,7 +200,7 @@ def time_oracle(budget_s: float = 15.0, seed_rows: int = 0, literal: bool = True
     # rows, for context: the same algorithmic FLOP count over its wall time
     lit_rows, lit_flops, lit_t = 0, 0.0, 0.0
     while literal and lit_t < min(5.0, budget_s / 3):
-        row = [(int(rng.integers(w.B)), int(rng.integers(min(w.Tq, 512))))]
+        row = [(int(rng.integers(w.B)), int(rng.integers(w.Tq)))]
         t0 = time.perf_counter()
         o.attention_rows(None, None, None, None, w.scale, row, prepared=prep, form="literal")
         lit_t += time.perf_counter() - t0
@@ -196,12 +209,163 @@ def time_oracle(budget_s: float = 15.0, seed_rows: int = 0, literal: bool = True
     lit = None if not literal else {
         "value": round(lit_flops / lit_t / 1e12, 6), "unit": "TFLOP/s",
         "sample": f"float64 C oracle, literal form (k, v rebuilt per key), {lit_rows} random "
-                  f"rows with i < 512 x {w.H} heads in {lit_t:.1f} s"}
+                  f"(b, i) rows over all i x {w.H} heads in {lit_t:.1f} s"}
     return value, {"kind": "oracle", "cores": cores, "literal_form": lit,
                    "sample": f"float64 C oracle (absorbed form, OpenMP over rows x heads), "
                              f"{done_rows} random (b, i) rows x {w.H} heads of the prefill "
                              f"attention B2 T4096 H32 d128 R512 in {t_total:.1f} s; algorithmic "
                              f"FLOPs of those rows / wall time"}
+
+
+def _omp_threads(n: int) -> None:
+    """Thread count of the oracle's OpenMP loops for the calling thread
+    (libgomp's omp_set_num_threads; the oracle library has loaded libgomp)."""
+    import ctypes
+    try:
+        ctypes.CDLL("libgomp.so.1").omp_set_num_threads(int(n))
+    except (OSError, AttributeError):
+        pass
+
+
+def _literal_flops(w) -> float:
+    """FLOPs of the literal form: k and v rebuilt (R*d multiply-adds each) for
+    every causal (query, key) pair and head, plus the q.k and p.v dot products."""
+    return (4.0 * w.rank * w.d + 4.0 * w.d) * w.pairs() * w.H
+
+
+def oracle_table(budget_s: float = 4.0):
+    """The float64 oracle on every workload, on this host's cores: the literal
+    form (k, v rebuilt per key), the absorbed form (C, pinned equal to it) and
+    the explicit numpy brute force (k, v materialised).  Each runs in full
+    where that takes a few seconds, else on a random sample of rows (or of
+    heads / sequences for the explicit form) timed for about ``budget_s``
+    seconds, with the full run's time extrapolated from the sample's rate.
+    Rates are algorithmic FLOPs (the metric's count) per second.  Single-core
+    times (OpenMP limited to one thread) for the three smaller workloads."""
+    import numpy as np
+    import oracle
+    from oracle import explicit
+    from latent_causal_attention_gb300.inputs import WORKLOADS, make_inputs
+
+    o = oracle.get()
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(77)
+
+    def row_flops(w, i):          # algorithmic FLOPs of row (b, i), all heads
+        t = w.Tkv - w.Tq + i
+        keys = (t + 1) if w.causal else w.Tkv
+        return 4.0 * w.rank * keys * w.H + 4.0 * w.H * w.rank * w.d
+
+    def rows_run(w, prep, form, budget):
+        """Random (b, i) rows over all i, timed until ``budget`` seconds have
+        passed; each call takes one row per core of ONE random head (a slice
+        of the prepared inputs), so that a call stays short even where a row
+        of every head would take minutes in the literal form."""
+        q, lat, wk, wv, (B, Tq, Tkv, H, d, R) = prep
+        heads = {}
+        n, fl, t = 0, 0.0, 0.0
+        while t < budget:
+            h = int(rng.integers(H))
+            if h not in heads:
+                heads[h] = (np.ascontiguousarray(q[:, :, h:h + 1]), lat,
+                            np.ascontiguousarray(wk[:, h:h + 1]),
+                            np.ascontiguousarray(wv[:, h:h + 1]), (B, Tq, Tkv, 1, d, R))
+            rows = [(int(rng.integers(w.B)), int(rng.integers(w.Tq))) for _ in range(cores)]
+            t0 = time.perf_counter()
+            o.attention_rows(None, None, None, None, w.scale, rows, prepared=heads[h], form=form)
+            t += time.perf_counter() - t0
+            fl += sum(row_flops(w, i) for _, i in rows) / w.H
+            n += len(rows)
+        return n, fl, t
+
+    def entry(w, fl_total, seconds, mode, sample):
+        return {"mode": mode, "seconds_full": round(seconds, 4),
+                "GFLOP_per_s": round(fl_total / seconds / 1e9, 3), "sample": sample}
+
+    table = {}
+    full_lit = {"tiny_f32", "proj_f32"}
+    full_abs = {"tiny_f32", "proj_f32", "mid_bf16", "decode_bf16"}
+    full_exp = {"tiny_f32", "proj_f32", "mid_bf16"}
+    for name in ("tiny_f32", "proj_f32", "mid_bf16", "prefill_bf16", "decode_bf16"):
+        w = WORKLOADS[name]
+        x = make_inputs(w)
+        fl = float(w.attention_flops())
+        rec = {"algorithmic_GFLOP": round(fl / 1e9, 6),
+               "literal_GFLOP": round(_literal_flops(w) / 1e9, 6)}
+        args = (x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"])
+        if name == "proj_f32":          # the workload starts with the projection
+            t0 = time.perf_counter()
+            wk2, wv2 = x["w_up_k"].reshape(w.rank, -1), x["w_up_v"].reshape(w.rank, -1)
+            o.project(x["hidden"], x["w_down"], wk2, wv2)
+            rec["projection"] = {"mode": "full", "seconds": round(time.perf_counter() - t0, 5),
+                                 "GFLOP": round(w.projection_flops(with_kv=True) / 1e9, 6)}
+        for form, full_set in (("literal", full_lit), ("absorbed", full_abs)):
+            fn = o.attention if form == "literal" else o.attention_absorbed
+            if name in full_set:
+                t0 = time.perf_counter()
+                fn(*args, w.scale, w.causal)
+                dt = time.perf_counter() - t0
+                rec[form] = entry(w, fl, dt, "full", "every output row")
+            else:
+                prep = o.prepare(*args)
+                n, f_s, t_s = rows_run(w, prep, form, budget_s)
+                rec[form] = entry(w, fl, fl / (f_s / t_s), "sampled",
+                                  f"{n} random (b, i, head) rows in {t_s:.1f} s; full time "
+                                  f"extrapolated from their rate")
+        # explicit numpy brute force: whole workload, or a subset of heads /
+        # sequences with the time scaled to the whole
+        if name in full_exp:
+            t0 = time.perf_counter()
+            explicit.attention(*args, w.scale, w.causal)
+            dt = time.perf_counter() - t0
+            rec["explicit"] = entry(w, fl, dt, "full", "every output row")
+        elif name == "prefill_bf16":
+            hs = [0, 9, 21, 31]
+            t0 = time.perf_counter()
+            for h in hs:
+                explicit.attention(x["q"][:, :, h:h + 1], x["kv_latent"], x["w_up_k"][:, h:h + 1],
+                                   x["w_up_v"][:, h:h + 1], w.scale, w.causal)
+            dt = (time.perf_counter() - t0) * w.H / len(hs)
+            rec["explicit"] = entry(w, fl, dt, "sampled",
+                                    f"heads {hs} of {w.H}; full time scaled by heads")
+        else:
+            bs = [0, 21, 42, 63]
+            t0 = time.perf_counter()
+            for b in bs:
+                explicit.attention(x["q"][b:b + 1], x["kv_latent"][b:b + 1], x["w_up_k"],
+                                   x["w_up_v"], w.scale, w.causal)
+            dt = (time.perf_counter() - t0) * w.B / len(bs)
+            rec["explicit"] = entry(w, fl, dt, "sampled",
+                                    f"sequences {bs} of {w.B}; full time scaled by sequences")
+        table[name] = rec
+    # one core: the C oracle's literal and absorbed forms on the small workloads
+    single = {}
+    _omp_threads(1)
+    try:
+        for name in ("tiny_f32", "proj_f32", "mid_bf16"):
+            w = WORKLOADS[name]
+            x = make_inputs(w)
+            args = (x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"])
+            fl = float(w.attention_flops())
+            rec = {}
+            for form in ("literal", "absorbed"):
+                if name == "mid_bf16":
+                    prep = o.prepare(*args)
+                    n, f_s, t_s = rows_run(w, prep, form, budget_s / 2)
+                    rec[form] = entry(w, fl, fl / (f_s / t_s), "sampled",
+                                      f"{n} random (b, i, head) rows, one thread, {t_s:.1f} s; "
+                                      f"full time extrapolated")
+                else:
+                    fn = o.attention if form == "literal" else o.attention_absorbed
+                    t0 = time.perf_counter()
+                    fn(*args, w.scale, w.causal)
+                    rec[form] = entry(w, fl, time.perf_counter() - t0, "full", "one thread")
+            single[name] = rec
+    finally:
+        _omp_threads(cores)
+    return {"kind": "oracle", "cores": cores, "workloads": table, "single_core": single,
+            "note": "float64 C oracle (OpenMP over rows x heads) and numpy float64 brute force "
+                    "(its BLAS threads), on this host's cores; a baseline, not the target"}
 
 
 def run_reference(args, rank: int, world: int):
@@ -243,7 +407,7 @@ def run_ours(args, rank: int, world: int):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    peaks, peak_kind = load_peaks()
+    peaks, peak_kind = load_peaks(torch.cuda.get_device_name(dev))
 
     w = WORKLOADS["prefill_bf16"]
     x = make_inputs(w)
@@ -385,6 +549,7 @@ def run_ours(args, rank: int, world: int):
                "GB_per_s": round(nbytes / (dms * 1e-3) / 1e9, 1),
                "ms": round(dms, 4), "algorithmic_bytes": nbytes,
                "frac_hbm": round(nbytes / (dms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+               "frac_hbm_spec": round(nbytes / (dms * 1e-3) / 1e9 / SPEC_PEAKS["hbm_gbs"], 4),
                "TFLOP_per_s": round(wd.attention_flops() / (dms * 1e-3) / 1e12, 2),
                "flash_ms": round(dflash, 4),
                "flash_frac_hbm": round(268435456 * 1.0 / (dflash * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -402,7 +567,9 @@ def run_ours(args, rank: int, world: int):
                "ms": round(mms, 4), "kernel_ms": round(mflash, 4),
                "TFLOP_per_s": round(wm.attention_flops() / (mms * 1e-3) / 1e12, 2),
                "frac_peak": round(wm.attention_flops() / (mms * 1e-3) / 1e12
-                                  / peaks["bf16_tflops"], 4)}
+                                  / peaks["bf16_tflops"], 4),
+               "frac_peak_spec": round(wm.attention_flops() / (mms * 1e-3) / 1e12
+                                       / SPEC_PEAKS["bf16_tflops"], 4)}
 
     # --- comparator: the same prefill step with k and v materialised (projection
     # with w_up_k / w_up_v outputs, then attention over explicit k, v)
@@ -451,14 +618,17 @@ def run_ours(args, rank: int, world: int):
                 "attention_frac_explicit_count": round(
                     xflops_attn / (xattn * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
 
+    small = time_small(dev) if not args.no_small else None
+
     if rank != 0:
         return
     flash_avg = statistics.mean(flash_ms)
     achieved = flops_flash / (flash_avg * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    cpu_val, cpu_detail = (None, None)
+    cpu_val, cpu_detail, otable = (None, None, None)
     if not args.no_cpu_baseline:
         cpu_val, cpu_detail = time_oracle(budget_s=15.0)
+        otable = oracle_table(budget_s=4.0)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -486,6 +656,9 @@ def run_ours(args, rank: int, world: int):
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                     "peak_spec": SPEC_PEAKS["bf16_tflops"],
+                     "frac_spec": round(achieved / SPEC_PEAKS["bf16_tflops"], 4),
+                     "peak_spec_source": SPEC_PEAKS["source"],
                      "flops_per_launch": flops_flash, "traffic": flash_traffic(),
                      "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -497,9 +670,11 @@ def run_ours(args, rank: int, world: int):
         "decode": dec,
         "mid": mid,
         "explicit_kv_comparator": expl,
+        "small_fp32_latency": small,
     }
     if cpu_val is not None:
         line["cpu_baseline"] = {**cpu_detail, "value": round(cpu_val, 6), "unit": "TFLOP/s"}
+        line["oracle_table"] = otable
     print(json.dumps(line), flush=True)
 
 
@@ -545,6 +720,79 @@ def time_attention_only(w, dev, flush, stream, n: int, warmup: int):
     return ms, kernel_ms
 
 
+def time_small(dev, n: int = 200, warmup: int = 20):
+    """Latency of the two fp32 workloads, in microseconds per call:
+    tiny_f32 (causal attention B2 T32 H4 d16 rank 24) and proj_f32 (projection
+    (4,96,256) -> rank 48 -> k, v, then attention H4 d32 on that latent).
+    ``device_us``: n back-to-back calls between two CUDA events, inputs
+    resident; ``call_us``: median of per-call event pairs; ``e2e_us``: median
+    wall time of one call through the public API with the inputs copied in
+    from pinned host memory and the result copied back, synchronised."""
+    import torch
+
+    import latent_causal_attention_gb300 as mla
+    from latent_causal_attention_gb300.inputs import WORKLOADS, make_inputs
+
+    res = {}
+    stream = torch.cuda.current_stream(dev)
+    for name in ("tiny_f32", "proj_f32"):
+        w = WORKLOADS[name]
+        x = make_inputs(w)
+        if name == "proj_f32":
+            x["w_up_k"] = x["w_up_k"].reshape(w.rank, w.H, w.d)
+            x["w_up_v"] = x["w_up_v"].reshape(w.rank, w.H, w.d)
+        d = {k: v.to(dev) for k, v in x.items()}
+        out = torch.empty(w.B, w.Tq, w.H, w.d, device=dev, dtype=torch.float32)
+        lat = torch.empty(w.B, w.Tkv, w.rank, device=dev, dtype=torch.float32)
+
+        def call(dd):
+            if name == "proj_f32":
+                mla.project(dd["hidden"], dd["w_down"], dd["w_up_k"].reshape(w.rank, -1),
+                            dd["w_up_v"].reshape(w.rank, -1), latent=lat)
+                mla.attention(dd["q"], lat, dd["w_up_k"], dd["w_up_v"], w.scale, True, out=out)
+            else:
+                mla.attention(dd["q"], dd["kv_latent"], dd["w_up_k"], dd["w_up_v"], w.scale,
+                              True, out=out)
+
+        for _ in range(warmup):
+            call(d)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            call(d)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        device_us = e0.elapsed_time(e1) * 1e3 / n
+        per = []
+        for _ in range(n // 4):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call(d)
+            b.record(stream)
+            b.synchronize()
+            per.append(a.elapsed_time(b) * 1e3)
+        host = {k: v.pin_memory() for k, v in x.items() if not (name == "proj_f32" and
+                                                                  k == "kv_latent")}
+        host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        e2e = []
+        for it in range(n // 4 + warmup):
+            t0 = time.perf_counter()
+            for k, v in host.items():
+                d[k].copy_(v, non_blocking=True)
+            call(d)
+            host_out.copy_(out, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+            if it >= warmup:
+                e2e.append((time.perf_counter() - t0) * 1e6)
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        res[name] = {"device_us": round(device_us, 2), "call_us": round(statistics.median(per), 2),
+                     "e2e_us": round(statistics.median(e2e), 2), "h2d_bytes": h2d,
+                     "d2h_bytes": host_out.numel() * 4,
+                     "flops": w.attention_flops() + w.projection_flops(with_kv=True)}
+    return res
+
+
 def run_attention_only(args, name: str):
     """Only one workload's attention (decode_bf16 or mid_bf16): warm-up, then
     timed calls with the L2 flushed between them; one JSON line.  A small
@@ -557,7 +805,7 @@ def run_attention_only(args, name: str):
     build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    peaks, _ = load_peaks()
+    peaks, _ = load_peaks(torch.cuda.get_device_name(dev))
     w = WORKLOADS[name]
     flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream(dev)
@@ -583,6 +831,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-explicit", action="store_true")
     ap.add_argument("--no-mid", action="store_true")
+    ap.add_argument("--no-small", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode attention (a driver for profiling its kernels)")
     ap.add_argument("--mid-only", action="store_true",

@@ -66,3 +66,30 @@ def test_peaks_come_from_the_measured_record_else_the_fallback(tmp_path, monkeyp
         json.dumps({"hbm_gbs": 6788.3, "bf16_tflops": 1909.8, "bf16_tflops_sustained": 1707.2}))
     peaks, kind = bench.load_peaks()
     assert kind == "measured" and peaks["bf16_tflops"] == 1909.8
+
+
+def test_peaks_record_of_another_gpu_is_not_used(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "MEASURED_PEAKS.json").write_text(
+        json.dumps({"hbm_gbs": 6758.2, "bf16_tflops": 1887.9, "gpu_name": "NVIDIA GB300"}))
+    assert bench.load_peaks("NVIDIA GB300")[1] == "measured"
+    peaks, kind = bench.load_peaks("NVIDIA B200")
+    assert kind.startswith("fallback") and peaks["bf16_tflops"] == 1900.0
+    assert bench.load_peaks()[1] == "measured"            # no device to compare with
+
+
+def test_spec_denominators_are_the_published_figures():
+    assert bench.SPEC_PEAKS["hbm_gbs"] == 8000.0
+    assert bench.SPEC_PEAKS["bf16_tflops"] == 2250.0 and "sparsity" in bench.SPEC_PEAKS["source"]
+
+
+def test_oracle_table_covers_every_workload_and_form():
+    t = bench.oracle_table(budget_s=0.05)
+    assert t["cores"] >= 1 and t["kind"] == "oracle"
+    assert set(t["workloads"]) == {"tiny_f32", "proj_f32", "mid_bf16", "prefill_bf16",
+                                   "decode_bf16"}
+    for name, rec in t["workloads"].items():
+        for form in ("literal", "absorbed", "explicit"):
+            assert rec[form]["seconds_full"] > 0 and rec[form]["mode"] in ("full", "sampled")
+    assert t["workloads"]["tiny_f32"]["literal"]["mode"] == "full"
+    assert set(t["single_core"]) == {"tiny_f32", "proj_f32", "mid_bf16"}
