@@ -179,27 +179,37 @@ __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t u, float s) {
   return pack_bf16x2(__uint_as_float(u << 16) * s, __uint_as_float(u & 0xffff0000u) * s);
 }
 
-// Pairwise (tree) max / sum of 32 values: log-depth dependency chains.
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Tree max / sum of 32 values: log-depth dependency chains; three-input max
+// and paired (float2) adds halve the instruction count.
 __device__ __forceinline__ float tree_max32(const float (&v)[32]) {
-  float a[16];
+  float a[11];
 #pragma unroll
-  for (int c = 0; c < 16; ++c) a[c] = fmaxf(v[c], v[c + 16]);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) a[c] = fmaxf(a[c], a[c + 8]);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) a[c] = fmaxf(a[c], a[c + 4]);
-  return fmaxf(fmaxf(a[0], a[2]), fmaxf(a[1], a[3]));
+  for (int c = 0; c < 10; ++c) a[c] = fmax3(v[3 * c], v[3 * c + 1], v[3 * c + 2]);
+  a[10] = fmaxf(v[30], v[31]);
+  const float b0 = fmax3(a[0], a[1], a[2]), b1 = fmax3(a[3], a[4], a[5]);
+  const float b2 = fmax3(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+  return fmaxf(fmax3(b0, b1, b2), b3);
 }
 
 __device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
-  float a[16];
+  float2 a[8];
 #pragma unroll
-  for (int c = 0; c < 16; ++c) a[c] = v[c] + v[c + 16];
+  for (int c = 0; c < 8; ++c)
+    a[c] = __fadd2_rn(make_float2(v[2 * c], v[2 * c + 1]),
+                      make_float2(v[2 * c + 16], v[2 * c + 17]));
 #pragma unroll
-  for (int c = 0; c < 8; ++c) a[c] = a[c] + a[c + 8];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) a[c] = a[c] + a[c + 4];
-  return (a[0] + a[2]) + (a[1] + a[3]);
+  for (int c = 0; c < 4; ++c) a[c] = __fadd2_rn(a[c], a[c + 4]);
+  a[0] = __fadd2_rn(a[0], a[2]);
+  a[1] = __fadd2_rn(a[1], a[3]);
+  a[0] = __fadd2_rn(a[0], a[1]);
+  return a[0].x + a[0].y;
 }
 
 // This thread's row of fp32 TMEM columns [src, src+n) times s, as bf16 pairs at
@@ -215,8 +225,10 @@ __device__ __forceinline__ void tmem_rows_to_bf16(uint32_t src, uint32_t dst, in
     for (int h = 0; h < 2; ++h) {
       float pk[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        pk[e] = __uint_as_float(pack_bf16x2(v[h][2 * e] * s, v[h][2 * e + 1] * s));
+      for (int e = 0; e < 16; ++e) {
+        const float2 t = __fmul2_rn(make_float2(v[h][2 * e], v[h][2 * e + 1]), make_float2(s, s));
+        pk[e] = __uint_as_float(pack_bf16x2(t.x, t.y));
+      }
       tmem_st16(dst + (c + 32 * h) / 2, pk);
     }
   }
@@ -714,12 +726,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                        : "=r"(u0), "=r"(u1), "=r"(u2), "=r"(u3)
                        : "r"(src + sw128_offset((uint32_t)r, (uint32_t)(half * 4 + c)))
                        : "memory");
-          const float2 f0 = unpack_half2(u0), f1 = unpack_half2(u1);
-          const float2 f2 = unpack_half2(u2), f3 = unpack_half2(u3);
-          s[8 * c] += f0.x; s[8 * c + 1] += f0.y;
-          s[8 * c + 2] += f1.x; s[8 * c + 3] += f1.y;
-          s[8 * c + 4] += f2.x; s[8 * c + 5] += f2.y;
-          s[8 * c + 6] += f3.x; s[8 * c + 7] += f3.y;
+          const float2 f[4] = {unpack_half2(u0), unpack_half2(u1), unpack_half2(u2),
+                               unpack_half2(u3)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 t = __fadd2_rn(make_float2(s[8 * c + 2 * e], s[8 * c + 2 * e + 1]), f[e]);
+            s[8 * c + 2 * e] = t.x;
+            s[8 * c + 2 * e + 1] = t.y;
+          }
         }
         // re-arm this buffer's barrier for tile j+kXBuf (its phase for tile j is complete)
         if (warp == 6 && lane == 0 && j + kXBuf < nt)
@@ -748,7 +762,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = grow_max ? ex2(m_run - m_new) : 1.f;   // m_run = -inf -> 0
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) s[c] = ex2(s[c] - m_use);
+      for (int c = 0; c < 16; ++c) {
+        const float2 t = __fadd2_rn(make_float2(s[2 * c], s[2 * c + 1]), make_float2(-m_use, -m_use));
+        s[2 * c] = ex2(t.x);
+        s[2 * c + 1] = ex2(t.y);
+      }
       l_half = l_half * alpha + tree_sum32(s);
       m_run = m_ref;
 
@@ -767,7 +785,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld16(tmem + lane_base + kTmemO + c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] *= alpha;
+          for (int e = 0; e < 8; ++e) {
+            const float2 t = __fmul2_rn(make_float2(o[2 * e], o[2 * e + 1]), make_float2(alpha, alpha));
+            o[2 * e] = t.x;
+            o[2 * e + 1] = t.y;
+          }
           tmem_st16(tmem + lane_base + kTmemO + c, o);
         }
         tmem_wait_st();
