@@ -32,8 +32,8 @@
 // the partial each receives).
 //
 // Warp roles (512 threads): warp 0 lane 0 = TMA producer (q' once, then a
-// 4-stage ring of latent tiles); warp 1 = TMEM owner, lane 0 issues the MMAs of
-// even tiles; warp 15 lane 0 issues those of odd tiles; warps 2-5 = partial-S
+// 4-stage ring of latent tiles); warp 1 = TMEM owner, lane 0 issues the S MMAs;
+// warp 15 lane 0 issues the O MMAs; warps 2-5 = partial-S
 // exchange (CTA pair only); warps 6-13 = softmax and epilogue, two warps per
 // row quadrant (each takes 32 of a tile's 64 keys and half of O_lat's
 // columns); warp 14 forwards receive-buffer releases to the peer (CTA pair
@@ -414,26 +414,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 || warp == 15) {
     // ======================= MMA issuers =======================
-    // Two issuing threads, lane 0 of warps 1 and 15 (different SM
-    // sub-partitions), take alternate tiles: issuer p owns S buffer p, P buffer
-    // p and tiles j = p (mod 2).  A thread that has just issued MMAs waits for
-    // the tensor core to take them before its next barrier test completes;
-    // with two issuers the other one keeps the tensor core fed meanwhile.
+    // Two issuing threads on different SM sub-partitions: lane 0 of warp 1
+    // issues every S(j) = q' L(j)^T (16 narrow N = 64 K-steps per tile, plus
+    // the fused kernel's prologue and epilogue MMAs), lane 0 of warp 15 every
+    // O(j) += P(j) L(j) (four long N = RC K-steps).  A thread that has just
+    // issued MMAs waits for the tensor core to take them before its next
+    // barrier test completes, so neither kind of MMA waits behind the other's
+    // issue; the O MMAs come from one thread in tile order, so the P.L products
+    // accumulate in tile order whatever the interleaving with the S MMAs.
     // O_lat was zeroed by the softmax warps, so every P.L accumulates.
-    // Per tile j, the four long O(j) += P(j) L(j) MMAs (N = RC) are interleaved
-    // with the narrow S(j+2) = q' L(j+2)^T MMAs (N = 64) of the same issuer,
-    // fully unrolled with descriptors advanced by constants.
-    const int par = warp == 1 ? 0 : 1;
+    const bool s_role = warp == 1;
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
       constexpr uint32_t idesc_o = make_idesc_bf16(kRows, kRC, false, true);
       constexpr int kSSteps = kRC / 16;            // K-steps of one S tile
-      constexpr int kSPerO = kSSteps / 4;          // S K-steps per O K-step
       const uint32_t l0 = smem_u32(sL), p0 = smem_u32(sP);
       const uint32_t tq = tmem + kTmemQ;
       bool ok = true;
       if constexpr (kFused) {
-        if (par == 0) {
+        if (s_role) {
           // q' (fp32, this CTA's rank columns) = q . w_up_k[:, h, c0:c0+RC]^T into O's columns
           ok = mbar_wait(&bars->pro_full, 0, 24, abort_flag);
           tc_fence_after();
@@ -457,68 +456,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   umma_bf16_ta((sbuf), tq + (k) * 8,                                                     \
                (bd) + (uint64_t)((((k) >> 2) * (kKeys * 128) + ((k) & 3) * 32) >> 4), idesc_s, \
                (k) > 0 ? 1u : 0u)
-      // Small scheduler over this issuer's tiles: S(js) as soon as latent tile
-      // js has landed and the readers of S(js-2) have let its buffer go; O(jo)
-      // as soon as P(jo) is written.  When both are ready, the narrow S K-steps
-      // are interleaved with the long O K-steps.
-      int js = par, jo = par;
-      const uint32_t sbuf = tmem + kTmemS + par * kKeys;
-      const uint32_t pbuf = p0 + par * kPBytes;
-      const unsigned long long t_start = globaltimer_ns();
-      unsigned spins = 0;
-      while (ok && jo < nt) {
-        const bool s_ready =
-            js < nt && mbar_test(smem_u32(&bars->l_full[js % kStages]), (js / kStages) & 1) &&
-            mbar_test(smem_u32(&bars->s_empty[par]), ((js >> 1) & 1) ^ 1);
-        // O(jo) also waits for O(jo-1) (the other issuer's) to complete, so the
-        // P.L products accumulate in tile order: the result does not depend on
-        // how the two issuers' instructions interleave
-        const bool o_ready =
-            jo < js && mbar_test(smem_u32(&bars->p_full[par]), (jo >> 1) & 1) &&
-            (jo == 0 || mbar_test(smem_u32(&bars->p_empty[par ^ 1]), ((jo - 1) >> 1) & 1));
-        if (!s_ready && !o_ready) {
-          // back off: this warp shares an SM sub-partition with softmax warps
-          __nanosleep(32);
-          if ((++spins & 255u) == 0 &&
-              (*abort_flag || globaltimer_ns() - t_start > kWaitLimitNs * 8)) {
-            report_error(kErrWaitTimeout | 21u);
-            *abort_flag = 1;
-            ok = false;
-          }
-          continue;
+      if (s_role) {
+        // S(j) as soon as latent tile j has landed and the readers of S(j-2)
+        // have let its buffer go
+        for (int js = 0; ok && js < nt; ++js) {
+          const int sb = js & 1;
+          ok = mbar_wait(&bars->l_full[js % kStages], (js / kStages) & 1, 22, abort_flag) &&
+               mbar_wait(&bars->s_empty[sb], ((js >> 1) & 1) ^ 1, 23, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t bds = make_sdesc_sw128(l0 + (js % kStages) * kLStage, 16, 1024);
+          const uint32_t sbuf = tmem + kTmemS + sb * kKeys;
+#pragma unroll
+          for (int k = 0; k < kSSteps; ++k) MLA_S_STEP(sbuf, bds, k);
+          umma_commit(&bars->s_full[sb]);
         }
-        tc_fence_after();
-        uint64_t bds = 0;
-        if (s_ready) bds = make_sdesc_sw128(l0 + (js % kStages) * kLStage, 16, 1024);
-        if (o_ready) {
-          const uint64_t ad = make_sdesc_sw128(pbuf, 16, 1024);
+      } else {
+        // O(j) as soon as P(j) is written; its completion frees P buffer j%2
+        // and latent stage j%kStages
+        for (int jo = 0; ok && jo < nt; ++jo) {
+          const int pb = jo & 1;
+          ok = mbar_wait(&bars->p_full[pb], (jo >> 1) & 1, 21, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t ad = make_sdesc_sw128(p0 + pb * kPBytes, 16, 1024);
           const uint64_t bdo = make_sdesc_sw128(
               l0 + (jo % kStages) * kLStage + (kExplicit ? kVOff : 0u), kKeys * 128, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
+          for (int kk = 0; kk < kKeys / 16; ++kk)
             umma_bf16(tmem + kTmemO, ad + (uint64_t)((kk * 32) >> 4),
                       bdo + (uint64_t)((kk * 2048) >> 4), idesc_o, 1u);
-            if (s_ready) {
-#pragma unroll
-              for (int q = 0; q < kSPerO; ++q) MLA_S_STEP(sbuf, bds, kk * kSPerO + q);
-            }
-          }
-          umma_commit(&bars->p_empty[par]);
+          umma_commit(&bars->p_empty[pb]);
           umma_commit(&bars->l_empty[jo % kStages]);
-          jo += 2;
-        } else {
-#pragma unroll
-          for (int k = 0; k < kSSteps; ++k) MLA_S_STEP(sbuf, bds, k);
-        }
-        if (s_ready) {
-          umma_commit(&bars->s_full[par]);
-          js += 2;
         }
       }
 #undef MLA_S_STEP
       umma_commit(&bars->o_last);
       if constexpr (kFused) {
-        if (par == 0) {
+        if (s_role) {
           // out_partial = O_lat(bf16, smem) . w_up_v[c0:c0+RC, h, :] into S's columns
           if (ok && mbar_wait(&bars->epi_a, 0, 25, abort_flag) &&
               mbar_wait(&bars->epi_w, 0, 26, abort_flag)) {
@@ -547,25 +522,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nt; ++j) {
         const int bi = j & 1, k = j >> 1;                 // S buffer and its use count
         const int xb = j % kXBuf, xk = j / kXBuf;         // receive buffer and its use count
+        // the peer's receive buffer first (normally free long before S is ready),
+        // so that the partial leaves as soon as S(j) is complete
+        if (!warp_wait<true>(&bars->x_empty[xb], xk & 1, 41, abort_flag)) break;
         if (!warp_wait(&bars->s_full[bi], k & 1, 40, abort_flag)) break;
         tc_fence_after();
-        if (!warp_wait<true>(&bars->x_empty[xb], xk & 1, 41, abort_flag)) break;
         const uint32_t dst = x_peer0 + xb * kXBytes;
         const uint32_t bar = xfull_peer0 + xb * 8;
+        float v[2][32];                           // my row, both 32-column halves in flight
+        tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys, v[0]);
+        tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys + 32, v[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_empty[bi]);          // S(j) is in registers
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {          // two 32-column halves, sent as fp16
-          float v[32];
-          tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys + hh * 32, v);
-          tmem_wait_ld();
+        for (int hh = 0; hh < 2; ++hh)            // sent as fp16
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            st_async_v4u(dst + sw128_offset(r, hh * 4 + c), pack_half2(v[8 * c], v[8 * c + 1]),
-                         pack_half2(v[8 * c + 2], v[8 * c + 3]),
-                         pack_half2(v[8 * c + 4], v[8 * c + 5]),
-                         pack_half2(v[8 * c + 6], v[8 * c + 7]), bar);
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->s_empty[bi]);
+            st_async_v4u(dst + sw128_offset(r, hh * 4 + c),
+                         pack_half2(v[hh][8 * c], v[hh][8 * c + 1]),
+                         pack_half2(v[hh][8 * c + 2], v[hh][8 * c + 3]),
+                         pack_half2(v[hh][8 * c + 4], v[hh][8 * c + 5]),
+                         pack_half2(v[hh][8 * c + 6], v[hh][8 * c + 7]), bar);
       }
       if constexpr (kFused) {
         // send the peer the half of this CTA's partial output that the peer stores,
