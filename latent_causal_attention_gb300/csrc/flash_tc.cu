@@ -147,7 +147,7 @@ static_assert(offsetof(Bars, q_ready) == 1 * 8 && offsetof(Bars, s_empty) == 12 
 __device__ __forceinline__ uint32_t bar_arrivals(int i, bool pair) {
   if (i == 1 || i == 14 || i == 15 || i == 33) return 256;   // q_ready, p_full, epi_a
   if (i == 12 || i == 13) return pair ? 384 : 256;           // s_empty (+ exchange warps)
-  if (i == 18) return 2;                                     // o_last: one per MMA issuer
+  if (i == 18) return pair ? 2 : 3;                          // o_last: one per MMA issuer
   if (i >= 27 && i <= 30) return 8;                          // x_consumed: softmax warps
   return 1;
 }
@@ -412,18 +412,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bars->q_full, 0, 12, nullptr);
       }
     }
-  } else if (warp == 1 || warp == 15) {
+  } else if (warp == 1 || warp == 15 || (warp == 2 && !a.pair)) {
     // ======================= MMA issuers =======================
-    // Two issuing threads on different SM sub-partitions: lane 0 of warp 1
-    // issues every S(j) = q' L(j)^T (16 narrow N = 64 K-steps per tile, plus
-    // the fused kernel's prologue and epilogue MMAs), lane 0 of warp 15 every
-    // O(j) += P(j) L(j) (four long N = RC K-steps).  A thread that has just
-    // issued MMAs waits for the tensor core to take them before its next
-    // barrier test completes, so neither kind of MMA waits behind the other's
-    // issue; the O MMAs come from one thread in tile order, so the P.L products
-    // accumulate in tile order whatever the interleaving with the S MMAs.
+    // Issuing threads (lane 0) on different SM sub-partitions.  Lane 0 of warp
+    // 1 issues the S(j) = q' L(j)^T MMAs (16 narrow N = 64 K-steps per tile;
+    // it also issues the fused kernel's prologue and epilogue MMAs); one other
+    // thread issues every O(j) += P(j) L(j) (four long N = RC K-steps).  A
+    // thread that has just issued MMAs waits for the tensor core to take them
+    // before its next barrier test completes, and a single thread issues N = 64
+    // MMAs more slowly than the tensor core runs them; so in a single CTA the
+    // S tiles are split between warp 1 (even j) and warp 15 (odd j) and warp 2,
+    // which has no exchange to do there, issues the O MMAs; in a CTA pair warp
+    // 15 issues the O MMAs.  The O MMAs come from one thread in tile order, so
+    // the P.L products accumulate in tile order whatever the interleaving.
     // O_lat was zeroed by the softmax warps, so every P.L accumulates.
-    const bool s_role = warp == 1;
+    const bool s_role = warp == 1 || (warp == 15 && !a.pair);
+    const int s_first = (warp == 15) ? 1 : 0, s_step = a.pair ? 1 : 2;
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
       constexpr uint32_t idesc_o = make_idesc_bf16(kRows, kRC, false, true);
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tq = tmem + kTmemQ;
       bool ok = true;
       if constexpr (kFused) {
-        if (s_role) {
+        if (warp == 1) {
           // q' (fp32, this CTA's rank columns) = q . w_up_k[:, h, c0:c0+RC]^T into O's columns
           ok = mbar_wait(&bars->pro_full, 0, 24, abort_flag);
           tc_fence_after();
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s_role) {
         // S(j) as soon as latent tile j has landed and the readers of S(j-2)
         // have let its buffer go
-        for (int js = 0; ok && js < nt; ++js) {
+        for (int js = s_first; ok && js < nt; js += s_step) {
           const int sb = js & 1;
           ok = mbar_wait(&bars->l_full[js % kStages], (js / kStages) & 1, 22, abort_flag) &&
                mbar_wait(&bars->s_empty[sb], ((js >> 1) & 1) ^ 1, 23, abort_flag);
@@ -493,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef MLA_S_STEP
       umma_commit(&bars->o_last);
       if constexpr (kFused) {
-        if (s_role) {
+        if (warp == 1) {
           // out_partial = O_lat(bf16, smem) . w_up_v[c0:c0+RC, h, :] into S's columns
           if (ok && mbar_wait(&bars->epi_a, 0, 25, abort_flag) &&
               mbar_wait(&bars->epi_w, 0, 26, abort_flag)) {
