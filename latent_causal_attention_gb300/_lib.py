@@ -12,7 +12,7 @@ MLA_F32, MLA_BF16 = 0, 1
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_NULL", 2: "MLA_ERR_SHAPE", 3: "MLA_ERR_DTYPE",
           4: "MLA_ERR_ALIGN", 5: "MLA_ERR_WORKSPACE", 6: "MLA_ERR_CUDA", 7: "MLA_ERR_TIMEOUT",
           8: "MLA_ERR_UNSUPPORTED"}
-OPT_ATTN_PATH, OPT_KV_SPLITS, OPT_PREFILL_FUSED, OPT_NUM_SMS = 0, 1, 2, 3
+OPT_ATTN_PATH, OPT_KV_SPLITS, OPT_PREFILL_FUSED, OPT_NUM_SMS, OPT_PERSISTENT = 0, 1, 2, 3, 4
 
 _lock = threading.Lock()
 _lib = None

@@ -998,6 +998,405 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Persistent single-CTA prefill (rank <= 256, d = 64): one resident CTA per
+// SM works through a list of (batch entry, head, 128-row block) items, so
+// that an item's set-up runs under the previous item's loop and epilogue.
+// The arithmetic of each item is the fused kernel's (same MMA sequences, same
+// softmax), so results are bit for bit those of flash_packed_kernel<RC, fused>.
+//
+//   shared memory: latent ring (4 x 32 KB), P (2 x 16 KB), staging (64 KB: the
+//     next item's q tile at +0 and w_up_k rows at +16 KB), row-max exchange;
+//   tensor memory: as the fused kernel (O_lat, two S buffers, q').
+//
+// Roles: warp 0 lane 0 TMA producer (q / w_up_k of each item as soon as the
+// previous item's absorption has read the staging, latent tiles into the
+// ring, w_up_v into the ring slot after the item's last tile); warp 1 lane 0
+// the absorption MMA, the S MMAs of even tiles and the output MMA; warp 15
+// lane 0 the S MMAs of odd tiles; warp 2 lane 0 the O MMAs; warps 6-13
+// softmax and epilogue.  Item boundary: the softmax warps normalise O_lat
+// into q''s columns (epi_a), warp 1 issues the output MMA and then the next
+// item's absorption into O's columns, the softmax warps read the output from
+// S's columns, store it, turn the next q' into bf16 and zero O (q_ready).
+//
+// Items are dealt in rounds of gridDim.x, heavy row blocks first, alternating
+// direction every round (CTA c takes items c, 2G-1-c, 2G+c, ...), which
+// balances the causal work between CTAs without a shared counter.  Ring slots
+// and S / P buffers are counted across items (a ring slot per latent tile and
+// one for the item's w_up_v); each per-item barrier completes once per item.
+// ---------------------------------------------------------------------------
+struct PBars {
+  uint64_t l_full[kStages];    // ring slot landed (latent tile; w_up_v slots: plain arrive)
+  uint64_t l_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_empty[2];         // softmax threads have read S
+  uint64_t p_full[2];          // softmax threads have written P
+  uint64_t p_empty[2];
+  uint64_t pro_full;           // the item's q tile and w_up_k rows staged (TMA)
+  uint64_t pro_done;           // absorption MMA done: staging free, q' (fp32) in O's columns
+  uint64_t q_ready;            // q' (bf16) in TMEM and O zeroed (softmax threads)
+  uint64_t o_last;             // every MMA of the item's loop has completed (three issuers)
+  uint64_t epi_a;              // normalised O_lat (bf16) in q''s columns (softmax threads)
+  uint64_t epi_done;           // output MMA done
+  uint64_t epi_w[2];           // w_up_v of item r staged (TMA), by item parity: the
+                               // producer may stage item r+1's before item r's is used
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+constexpr int kPNumBars = 24;
+static_assert(offsetof(PBars, s_empty) == 10 * 8 && offsetof(PBars, p_full) == 12 * 8 &&
+                  offsetof(PBars, q_ready) == 18 * 8 && offsetof(PBars, o_last) == 19 * 8 &&
+                  offsetof(PBars, epi_a) == 20 * 8 && offsetof(PBars, epi_w) == 22 * 8,
+              "persistent barrier indices");
+static_assert(sizeof(PBars) <= kBarBytes, "persistent barrier block");
+
+__device__ __forceinline__ uint32_t pbar_arrivals(int i) {
+  if (i == 10 || i == 11 || i == 12 || i == 13 || i == 18 || i == 20) return 256;
+  if (i == 19) return 3;
+  return 1;
+}
+
+struct PItem {
+  int b, head, row0, nt;
+};
+
+// Item of round r for this CTA (false when the list is exhausted).
+__device__ __forceinline__ bool persist_item(const FlashArgs& a, int r, PItem& it) {
+  const int G = (int)gridDim.x, c = (int)blockIdx.x;
+  const int w = r * G + ((r & 1) ? G - 1 - c : c);
+  const int per_rb = a.B * a.H;
+  if (w >= a.row_blocks * per_rb) return false;
+  const int rb = a.row_blocks - 1 - w / per_rb;
+  it.b = (w % per_rb) / a.H;
+  it.head = w % a.H;
+  it.row0 = rb * kRows;
+  const int last_row = min(it.row0 + kRows, a.Tq) - 1;
+  const int t_max = a.Tkv - a.Tq + last_row;
+  const int kv_len = a.causal ? min(t_max + 1, a.Tkv) : a.Tkv;
+  it.nt = (kv_len + kKeys - 1) / kKeys;
+  return true;
+}
+
+template <int kRC>
+__global__ void __launch_bounds__(kThreads, 1)
+    flash_persistent_kernel(const __grid_constant__ CUtensorMap mapQ,
+                            const __grid_constant__ CUtensorMap mapL,
+                            const __grid_constant__ CUtensorMap mapWk,
+                            const __grid_constant__ CUtensorMap mapWv, FlashArgs a) {
+  extern __shared__ uint8_t flash_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(flash_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sL = smem + kOffL;
+  uint8_t* sP = smem + kOffP;
+  uint8_t* sX = smem + kOffX;                 // staging: q tile at +0, w_up_k at +16 KB
+  PBars* bars = reinterpret_cast<PBars*>(smem + kOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+  constexpr int RC = kRC;
+  constexpr uint32_t kWkOff = kRows * 128;    // 16 KB: after the q tile (d = 64)
+  static_assert(kWkOff + RC * 128 <= kXBuf * kXBytes, "persistent staging");
+  static_assert(RC * 128 <= kLStage, "w_up_v slot");
+
+  grid_dep_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    uint64_t* const bar0 = &bars->l_full[0];
+    for (int i = lane; i < kPNumBars; i += 32) mbar_init(bar0 + i, pbar_arrivals(i));
+    if (lane == 0) bars->abort_flag = 0;
+    fence_mbarrier_init_cluster();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  grid_dep_wait();        // set-up above overlaps the previous kernel's tail
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      prefetch_tensormap(&mapQ);
+      prefetch_tensormap(&mapL);
+      int R = 0, hi = 0, armed = -1, armed_w = -1;   // next ring slot, slots armed, last items staged
+      bool ok = true;
+      PItem it;
+      for (int r = 0; ok && persist_item(a, r, it); ++r) {
+        // the staging is free once the previous item's absorption has read it
+        if (r > 0 && !(ok = mbar_wait(&bars->pro_done, (r - 1) & 1, 60, abort_flag))) break;
+        mbar_arrive_expect_tx(&bars->pro_full, (uint32_t)(kRows * 128 + RC * 128));
+        tma_load_3d(sX, &mapQ, &bars->pro_full, 0, it.head, it.b * a.Tq + it.row0);
+        tma_load_3d(sX + kWkOff, &mapWk, &bars->pro_full, 0, it.head, 0);
+        armed = r;
+        for (int j = 0; j < it.nt; ++j) {
+          const int slot = R + j, st = slot % kStages;
+          if (!(ok = mbar_wait(&bars->l_empty[st], ((slot / kStages) & 1) ^ 1, 61, abort_flag)))
+            break;
+          mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(kKeys * RC * 2));
+          for (int kc = 0; kc < RC / 64; ++kc)
+            tma_load_3d(sL + st * kLStage + kc * (kKeys * 128), &mapL, &bars->l_full[st], 64 * kc,
+                        j * kKeys, it.b);
+          hi = slot + 1;
+        }
+        if (!ok) break;
+        // w_up_v rows of the head (MN-major B of the output MMA) into the next slot
+        const int slot = R + it.nt, st = slot % kStages;
+        if (!(ok = mbar_wait(&bars->l_empty[st], ((slot / kStages) & 1) ^ 1, 62, abort_flag)))
+          break;
+        mbar_arrive(&bars->l_full[st]);              // the slot's phase, nothing to wait for
+        uint64_t* ew = &bars->epi_w[r & 1];
+        mbar_arrive_expect_tx(ew, (uint32_t)(RC * 128));
+        for (int kb = 0; kb < RC / 64; ++kb)
+          tma_load_3d(sL + st * kLStage + kb * (64 * 128), &mapWv, ew, 0, it.head, 64 * kb);
+        hi = slot + 1;
+        armed_w = r;
+        R += it.nt + 1;
+      }
+      if (!ok) {
+        // leave no copy in flight: the last slot of every stage and the last
+        // item's staging (bounded waits)
+        for (int slot = max(0, hi - kStages); slot < hi; ++slot)
+          mbar_wait(&bars->l_full[slot % kStages], (slot / kStages) & 1, 63, nullptr);
+        if (armed >= 0) mbar_wait(&bars->pro_full, armed & 1, 63, nullptr);
+        if (armed_w >= 0) mbar_wait(&bars->epi_w[armed_w & 1], (armed_w >> 1) & 1, 63, nullptr);
+      }
+    }
+  } else if (warp == 1 || warp == 15 || warp == 2) {
+    // ======================= MMA issuers =======================
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
+      constexpr uint32_t idesc_o = make_idesc_bf16(kRows, kRC, false, true);
+      constexpr uint32_t idesc_q = make_idesc_bf16(kRows, kRC, false, false);
+      constexpr uint32_t idesc_v = make_idesc_bf16(kRows, 64, false, true);
+      constexpr int kSSteps = kRC / 16;
+      const uint32_t l0 = smem_u32(sL), p0 = smem_u32(sP), x0 = smem_u32(sX);
+      const uint32_t tq = tmem + kTmemQ;
+      // output MMA of an item: out = O_lat(bf16, q''s columns) . w_up_v into S's columns
+      auto output_mma = [&](int r, int wslot) -> bool {
+        if (!mbar_wait(&bars->epi_a, r & 1, 64, abort_flag) ||
+            !mbar_wait(&bars->epi_w[r & 1], (r >> 1) & 1, 65, abort_flag)) {
+          umma_commit(&bars->epi_done);
+          return false;
+        }
+        tc_fence_after();
+        const uint64_t bv = make_sdesc_sw128(l0 + (wslot % kStages) * kLStage, kLStage, 1024);
+#pragma unroll
+        for (int k = 0; k < kRC / 16; ++k)
+          umma_bf16_ta(tmem + kTmemS, tq + k * 8, bv + (uint64_t)((k * 2048) >> 4), idesc_v,
+                       k > 0 ? 1u : 0u);
+        umma_commit(&bars->epi_done);
+        umma_commit(&bars->l_empty[wslot % kStages]);
+        return true;
+      };
+      int T = 0, R = 0, prev_wslot = -1;
+      bool ok = true;
+      PItem it;
+      int r = 0;
+      for (; ok && persist_item(a, r, it); ++r) {
+        if (warp == 1) {
+          if (r > 0) ok = output_mma(r - 1, prev_wslot);
+          // this item's q' (fp32) = q . w_up_k[:, h, :]^T into O's columns, which the
+          // previous item's normalisation has read (epi_a, waited just above)
+          ok = ok && mbar_wait(&bars->pro_full, r & 1, 66, abort_flag);
+          if (ok) {
+            tc_fence_after();
+            const uint64_t aq = make_sdesc_sw128(x0, 16, 1024);
+            const uint64_t bw = make_sdesc_sw128(x0 + kWkOff, 16, 1024);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              umma_bf16(tmem + kTmemO, aq + (uint64_t)((k * 32) >> 4),
+                        bw + (uint64_t)((k * 32) >> 4), idesc_q, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars->pro_done);
+        }
+        ok = ok && mbar_wait(&bars->q_ready, r & 1, 67, abort_flag);
+        tc_fence_after();
+        if (warp != 2) {
+          // S(j) = q' L(j)^T for this thread's tiles (global tile count even / odd)
+          const int par = warp == 1 ? 0 : 1;
+          for (int j = 0; ok && j < it.nt; ++j) {
+            const int g = T + j;
+            if ((g & 1) != par) continue;
+            const int slot = R + j, st = slot % kStages;
+            ok = mbar_wait(&bars->l_full[st], (slot / kStages) & 1, 68, abort_flag) &&
+                 mbar_wait(&bars->s_empty[g & 1], ((g >> 1) & 1) ^ 1, 69, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t bds = make_sdesc_sw128(l0 + st * kLStage, 16, 1024);
+            const uint32_t sbuf = tmem + kTmemS + (g & 1) * kKeys;
+#pragma unroll
+            for (int k = 0; k < kSSteps; ++k)
+              umma_bf16_ta(sbuf, tq + k * 8,
+                           bds + (uint64_t)((((k) >> 2) * (kKeys * 128) + ((k) & 3) * 32) >> 4),
+                           idesc_s, k > 0 ? 1u : 0u);
+            umma_commit(&bars->s_full[g & 1]);
+          }
+        } else {
+          // O(j) += P(j) L(j), in tile order from this one thread
+          for (int j = 0; ok && j < it.nt; ++j) {
+            const int g = T + j, pb = g & 1;
+            const int st = (R + j) % kStages;
+            if (!(ok = mbar_wait(&bars->p_full[pb], (g >> 1) & 1, 70, abort_flag))) break;
+            tc_fence_after();
+            const uint64_t ad = make_sdesc_sw128(p0 + pb * kPBytes, 16, 1024);
+            const uint64_t bdo = make_sdesc_sw128(l0 + st * kLStage, kKeys * 128, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kKeys / 16; ++kk)
+              umma_bf16(tmem + kTmemO, ad + (uint64_t)((kk * 32) >> 4),
+                        bdo + (uint64_t)((kk * 2048) >> 4), idesc_o, 1u);
+            umma_commit(&bars->p_empty[pb]);
+            umma_commit(&bars->l_empty[st]);
+          }
+        }
+        umma_commit(&bars->o_last);
+        prev_wslot = R + it.nt;
+        T += it.nt;
+        R += it.nt + 1;
+      }
+      if (warp == 1 && ok && r > 0) output_mma(r - 1, prev_wslot);
+    }
+  } else if (warp >= 6 && warp < 14) {
+    // ======================= softmax / epilogue =======================
+    const int qd = warp & 3;
+    const int half = (warp - 6) >> 2;
+    const int r_ = qd * 32 + lane;                // row within the tile
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    float* red = reinterpret_cast<float*>(smem + kOffRed);
+    const uint32_t bar_id = 1u + (uint32_t)qd;
+    const int oc0 = half * (RC / 2);
+    int T = 0;
+    bool ok = true;
+    PItem it;
+    for (int r = 0; ok && persist_item(a, r, it); ++r) {
+      const int grow = it.row0 + r_;
+      const bool row_valid = grow < a.Tq;
+      const int t_row = a.Tkv - a.Tq + (row_valid ? grow : 0);
+      // q' (fp32 in O's columns) -> scaled by scale*log2(e) -> bf16 pairs in TMEM;
+      // q''s columns are free once the previous item's output MMA has read them
+      if (!(ok = warp_wait(&bars->pro_done, r & 1, 71, abort_flag))) break;
+      tc_fence_after();
+      tmem_rows_to_bf16(tmem + lane_base + kTmemO + oc0, tmem + lane_base + kTmemQ + oc0 / 2,
+                        RC / 2, a.qscale);
+      {
+        float z[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[e] = 0.f;
+        for (int c = oc0; c < oc0 + RC / 2; c += 32) tmem_st32(tmem + lane_base + kTmemO + c, z);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->q_ready);
+
+      float m_run = -INFINITY, l_half = 0.f;
+      for (int j = 0; j < it.nt; ++j) {
+        const int g = T + j, bi = g & 1, k = g >> 1;
+        float s[32];
+        if (!(ok = warp_wait(&bars->s_full[bi], k & 1, 72, abort_flag))) break;
+        tc_fence_after();
+        tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys + half * 32, s);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_empty[bi]);
+        const int key0 = j * kKeys + half * 32;
+        const int lim = a.causal ? min(t_row + 1, a.Tkv) : a.Tkv;
+        if (!row_valid || key0 + 32 > lim) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (!row_valid || key0 + c >= lim) s[c] = -INFINITY;
+        }
+        const float mx_half = tree_max32(s);
+        red[half * 128 + r_] = mx_half;
+        named_bar_sync(bar_id, 64);
+        const float mx = fmaxf(mx_half, red[(half ^ 1) * 128 + r_]);
+        named_bar_sync(bar_id, 64);
+        const float m_new = fmaxf(m_run, mx);
+        const bool grow_max = m_new > m_run + kRescaleThreshold;
+        const float m_ref = grow_max ? m_new : m_run;
+        const float alpha = grow_max ? ex2(m_run - m_new) : 1.f;
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float2 t = __fadd2_rn(make_float2(s[2 * c], s[2 * c + 1]),
+                                      make_float2(-m_use, -m_use));
+          s[2 * c] = ex2(t.x);
+          s[2 * c + 1] = ex2(t.y);
+        }
+        l_half = l_half * alpha + tree_sum32(s);
+        m_run = m_ref;
+        if (!(ok = warp_wait(&bars->p_empty[bi], (k & 1) ^ 1, 73, abort_flag))) break;
+        if (__any_sync(0xffffffffu, grow_max && j > 0)) {
+          if (!(ok = warp_wait(&bars->p_empty[(g - 1) & 1], ((g - 1) >> 1) & 1, 74, abort_flag)))
+            break;
+          tc_fence_after();
+          for (int c = oc0; c < oc0 + RC / 2; c += 16) {
+            float o[16];
+            tmem_ld16(tmem + lane_base + kTmemO + c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float2 t = __fmul2_rn(make_float2(o[2 * e], o[2 * e + 1]),
+                                          make_float2(alpha, alpha));
+              o[2 * e] = t.x;
+              o[2 * e + 1] = t.y;
+            }
+            tmem_st16(tmem + lane_base + kTmemO + c, o);
+          }
+          tmem_wait_st();
+        }
+        const uint32_t pb = smem_u32(sP + bi * kPBytes);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          st_shared_v4(pb + sw128_offset(r_, half * 4 + c), pack_bf16x2(s[8 * c], s[8 * c + 1]),
+                       pack_bf16x2(s[8 * c + 2], s[8 * c + 3]),
+                       pack_bf16x2(s[8 * c + 4], s[8 * c + 5]),
+                       pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[bi]);
+      }
+      if (!ok) break;
+
+      // ---------------- epilogue of the item ----------------
+      red[half * 128 + r_] = l_half;
+      named_bar_sync(bar_id, 64);
+      const float l_run = red[r_] + red[128 + r_];
+      named_bar_sync(bar_id, 64);              // red[] is reused by the next item
+      if (!(ok = warp_wait(&bars->o_last, r & 1, 75, abort_flag))) break;
+      tc_fence_after();
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      tmem_rows_to_bf16(tmem + lane_base + kTmemO + oc0, tmem + lane_base + kTmemQ + oc0 / 2,
+                        RC / 2, inv);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->epi_a);
+      if (!(ok = warp_wait(&bars->epi_done, r & 1, 76, abort_flag))) break;
+      tc_fence_after();
+      // out[b, i, h, half*32 .. +32]: my row's half of the head's 64 values
+      float v[32];
+      tmem_ld32(tmem + lane_base + kTmemS + half * 32, v);
+      tmem_wait_ld();
+      if (row_valid) {
+        const int64_t orow = (((int64_t)it.b * a.Tq + grow) * a.H + it.head) * 64 + half * 32;
+        if (a.out_bf16) {
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        } else {
+          float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+      T += it.nt;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
 // Split-KV merge: out[r,:] = sum_p 2^(m_p - M) o_p[r,:] / sum_p 2^(m_p - M) l_p
 // (page "Kimi-K2.6 l2_p29", online softmax, applied to whole partitions).
 // One block of width/4 threads per row, float4 per thread.
@@ -1122,6 +1521,44 @@ cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
       return launch_flash_rc<192, kModeFused>(mapQ, mapL, mapWk, mapWv, mapO, args, stream);
     case 256:
       return launch_flash_rc<256, kModeFused>(mapQ, mapL, mapWk, mapWv, mapO, args, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int kRC>
+static cudaError_t launch_persistent_rc(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                        const CUtensorMap& mapWk, const CUtensorMap& mapWv,
+                                        const FlashArgs& args, int num_ctas,
+                                        cudaStream_t stream) {
+  auto kern = flash_persistent_kernel<kRC>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_ctas, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flash_persistent(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                    const CUtensorMap& mapWk, const CUtensorMap& mapWv,
+                                    const FlashArgs& args, int num_ctas, cudaStream_t stream) {
+  if (args.pair || args.d != 64 || args.cu_q != nullptr || num_ctas <= 0)
+    return cudaErrorInvalidValue;
+  switch (args.RC) {
+    case 64: return launch_persistent_rc<64>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
+    case 128: return launch_persistent_rc<128>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
+    case 192: return launch_persistent_rc<192>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
+    case 256: return launch_persistent_rc<256>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }

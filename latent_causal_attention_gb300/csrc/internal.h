@@ -85,6 +85,14 @@ cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                const CUtensorMap& mapO, const FlashArgs& args,
                                cudaStream_t stream);
 
+// Persistent single-CTA prefill (rank <= 256, d = 64, dense batch): num_ctas
+// resident CTAs work through the (batch entry, head, 128-row block) items; same
+// tensor maps as the fused prefill minus the output map (rows are stored
+// directly); results bitwise equal to launch_flash_fused's.
+cudaError_t launch_flash_persistent(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                    const CUtensorMap& mapWk, const CUtensorMap& mapWv,
+                                    const FlashArgs& args, int num_ctas, cudaStream_t stream);
+
 cudaError_t launch_merge_partials(const float* m_l, int ml_stride, const float* l, const float* o,
                                   void* out, int parts, int rows, int width, int out_bf16,
                                   cudaStream_t stream);

@@ -69,6 +69,7 @@ static int g_attn_path = 0;     // 0 auto, 1 warp, 2 tensor core
 static int g_kv_splits = 0;     // 0 auto
 static int g_prefill_fused = 1; // 1: one fused kernel per head for long prefill
 static int g_num_sms = 0;       // > 0: SM count the planner assumes (0: the device's own)
+static int g_persistent = 1;    // 1: persistent kernel for single-CTA prefill with d = 64
 static void** g_stage_events = nullptr;
 static int g_stage_events_n = 0;
 static unsigned long long g_launches = 0;
@@ -232,6 +233,10 @@ mla_status_t mla_set_option(int option, int64_t value) {
       if (value < 0 || value > 4096) return MLA_ERR_SHAPE;
       g_num_sms = (int)value;
       return MLA_OK;
+    case MLA_OPT_PERSISTENT:
+      if (value < 0 || value > 1) return MLA_ERR_SHAPE;
+      g_persistent = (int)value;
+      return MLA_OK;
     default:
       return MLA_ERR_UNSUPPORTED;
   }
@@ -391,6 +396,16 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
     fa.row_blocks = p.row_blocks; fa.splits = 1; fa.causal = causal ? 1 : 0;
     fa.d = d; fa.qscale = scale * 1.4426950408889634f; fa.out = out;
     fa.out_bf16 = out_dtype == MLA_BF16;
+    if (g_persistent && !p.pair && d == 64) {
+      // one resident CTA per SM works through the (b, head, row block) items
+      const int64_t items = (int64_t)p.row_blocks * B * H;
+      const int ctas = (int)(items < planner_sm_count() ? items : planner_sm_count());
+      if (staged(1, stream, [&] {
+            return launch_flash_persistent(mQ, mL, mWk, mWv, fa, ctas, stream);
+          }) != cudaSuccess)
+        return MLA_ERR_CUDA;
+      return MLA_OK;
+    }
     if (staged(1, stream,
                [&] { return launch_flash_fused(mQ, mL, mWk, mWv, mO, fa, stream); }) !=
         cudaSuccess)

@@ -530,3 +530,34 @@ def test_calls_capture_into_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
     assert mla.device_error() == 0
+
+
+# ------------------------------------------- persistent single-CTA prefill
+PERSIST = [
+    dict(B=2, Tq=300, Tkv=300, H=4, d=64, rank=256, causal=True),     # ragged row blocks
+    dict(B=1, Tq=200, Tkv=700, H=3, d=64, rank=128, causal=True),     # chunked prefill
+    dict(B=3, Tq=128, Tkv=128, H=2, d=64, rank=64, causal=False),     # no mask
+    dict(B=1, Tq=1024, Tkv=1024, H=40, d=64, rank=192, causal=True),  # 320 items: several rounds
+]
+
+
+@pytest.mark.parametrize("shape", PERSIST, ids=lambda s: "x".join(str(v) for v in s.values()))
+def test_persistent_prefill_matches_per_block_kernel(oracle, shape):
+    """Long prefill with rank <= 256 and d = 64 runs one resident CTA per SM
+    over all row blocks; it does the same arithmetic as one CTA per row block,
+    so the two agree bit for bit, and both match the oracle."""
+    w = custom_workload("persist", dtype="bf16", **shape)
+    x = make_inputs(w, seed=13)
+    outs = {}
+    for persistent in (1, 0):
+        mla.set_option(_lib.OPT_PERSISTENT, persistent)
+        try:
+            outs[persistent] = (run_attention(x, w), run_attention(x, w, out_dtype=torch.bfloat16))
+            torch.cuda.synchronize()
+        finally:
+            mla.set_option(_lib.OPT_PERSISTENT, 1)
+    assert torch.equal(outs[1][0], outs[0][0]) and torch.equal(outs[1][1], outs[0][1])
+    ref = oracle.attention(x["q"], x["kv_latent"], x["w_up_k"], x["w_up_v"], w.scale, w.causal)
+    assert_bf16_close(outs[1][0], ref, f"persistent {shape}")
+    assert_bf16_close(outs[1][1].float(), ref, f"persistent {shape} bf16 out")
+    assert mla.device_error() == 0
