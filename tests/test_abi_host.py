@@ -144,6 +144,10 @@ def test_options(lib):
     assert lib.mla_set_option(0, 3) == 2
     assert lib.mla_set_option(99, 0) == 8
     assert lib.mla_set_option(0, 0) == 0
+    for opt in (_lib.OPT_PREFILL_FUSED, _lib.OPT_PERSISTENT):
+        assert lib.mla_set_option(opt, 2) == 2
+        assert lib.mla_set_option(opt, -1) == 2
+        assert lib.mla_set_option(opt, 1) == 0
     assert lib.mla_merge_partials(None, P, P, P, 1, 1, 4, 0, None) == 1
     assert lib.mla_merge_partials(P, P, P, P, 1, 1, 6, 0, None) == 2
 
