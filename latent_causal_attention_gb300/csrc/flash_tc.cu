@@ -38,6 +38,7 @@
 // row quadrant (each takes 32 of a tile's 64 keys and half of O_lat's
 // columns); warp 14 forwards receive-buffer releases to the peer (CTA pair
 // only).  Warp w reads TMEM lanes 32*(w%4)..+31.
+#include <atomic>
 #include <cuda_bf16.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -1059,9 +1060,9 @@ struct PItem {
   int b, head, row0, nt;
 };
 
-// Item of round r for this CTA (false when the list is exhausted).
-__device__ __forceinline__ bool persist_item(const FlashArgs& a, int r, PItem& it) {
-  const int G = (int)gridDim.x, c = (int)blockIdx.x;
+// Item of round r for worker c of G (a CTA, or a CTA pair); false when the
+// list is exhausted.
+__device__ __forceinline__ bool persist_item(const FlashArgs& a, int r, int G, int c, PItem& it) {
   const int w = r * G + ((r & 1) ? G - 1 - c : c);
   const int per_rb = a.B * a.H;
   if (w >= a.row_blocks * per_rb) return false;
@@ -1118,7 +1119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int R = 0, hi = 0, armed = -1, armed_w = -1;   // next ring slot, slots armed, last items staged
       bool ok = true;
       PItem it;
-      for (int r = 0; ok && persist_item(a, r, it); ++r) {
+      for (int r = 0; ok && persist_item(a, r, (int)gridDim.x, (int)blockIdx.x, it); ++r) {
         // the staging is free once the previous item's absorption has read it
         if (r > 0 && !(ok = mbar_wait(&bars->pro_done, (r - 1) & 1, 60, abort_flag))) break;
         mbar_arrive_expect_tx(&bars->pro_full, (uint32_t)(kRows * 128 + RC * 128));
@@ -1189,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       PItem it;
       int r = 0;
-      for (; ok && persist_item(a, r, it); ++r) {
+      for (; ok && persist_item(a, r, (int)gridDim.x, (int)blockIdx.x, it); ++r) {
         if (warp == 1) {
           if (r > 0) ok = output_mma(r - 1, prev_wslot);
           // this item's q' (fp32) = q . w_up_k[:, h, :]^T into O's columns, which the
@@ -1264,7 +1265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int T = 0;
     bool ok = true;
     PItem it;
-    for (int r = 0; ok && persist_item(a, r, it); ++r) {
+    for (int r = 0; ok && persist_item(a, r, (int)gridDim.x, (int)blockIdx.x, it); ++r) {
       const int grow = it.row0 + r_;
       const bool row_valid = grow < a.Tq;
       const int t_row = a.Tkv - a.Tq + (row_valid ? grow : 0);
@@ -1394,6 +1395,684 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Persistent CTA-pair prefill (rank 384 or 512: each CTA of a cluster of two
+// holds RC = rank / 2 rank columns; d = 64 or 128): one resident pair per two
+// SMs works through the (batch entry, head, 128-row block) items in the order
+// of the single-CTA kernel, and both CTAs of a pair take the same items.  The
+// arithmetic of an item is the fused kernel's (same MMA sequences, softmax,
+// partial-S and partial-output exchange), so the results are bit for bit those
+// of flash_packed_kernel<RC, fused> with a CTA pair.
+//
+// What changes is the item boundary.  The fused kernel ends an item with the
+// normalisation, the output MMA, the exchange of the partial outputs and the
+// stores, and the next CTA then starts with its set-up, the q / w_up_k loads
+// and the absorption.  Here the output MMA of item r and the absorption of
+// item r+1 are issued back to back, and the exchange and stores of item r's
+// output run while item r+1's first score tile is computed and exchanged.
+//
+// Shared memory per item:
+//   ring slots (32 KB each, counted across items): w_up_k of the head (one
+//     slot per 64 d columns, the absorption's B), the latent tiles, w_up_v
+//     (one slot per 64 d columns, the output MMA's B);
+//   receive buffers: with T the global index of the item's first tile, the
+//     q tile of the item sits in buffers T%4 and (T+1)%4 (one per 64 d
+//     columns) and the peer's partial output of the previous item in buffers
+//     (T+2)%4 (fp16 rows) and (T+3)%4 (row factors); these are the buffers of
+//     the previous item's last four tiles, so they are free before the item
+//     boundary.  Tile g uses buffer g%4, as in the fused kernel.
+//
+// Receive-buffer releases: the peer writes a buffer (a partial S tile or a
+// partial output) only after the release of its previous write, forwarded by
+// warp 14 from the local consumers (x_consumed -> the peer's x_empty), so the
+// n-th write into a buffer waits for the n-th release; both sides keep the
+// parity of each buffer's next release in a 4-bit mask.  A buffer that is to
+// take the next item's q tile is not released after its last use: its release
+// waits until the absorption has read the q tile.
+//
+// Roles: warp 0 lane 0 ring producer; warp 1 lane 0 absorption, S MMAs and
+// output MMA; warp 15 lane 0 O MMAs; warps 2-5 partial-S exchange and the
+// partial-output send; warp 14 lane 0 release forwarding and the q-tile loads
+// (it sees every consumption of the receive buffers in order); warps 6-13
+// softmax, normalisation, the q' conversion and the stores.
+// ---------------------------------------------------------------------------
+struct QBars {
+  uint64_t l_full[kStages];    // ring slot landed (latent tile, w_up_k or w_up_v rows)
+  uint64_t l_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_empty[2];         // softmax and exchange threads have read S
+  uint64_t p_full[2];
+  uint64_t p_empty[2];
+  uint64_t pro_full;           // the item's q tile staged in the receive buffers (TMA)
+  uint64_t pro_done;           // absorption MMA done
+  uint64_t q_ready;            // q' in TMEM, O zeroed, the previous output read (softmax + exchange)
+  uint64_t o_last;             // the item's S and O MMAs have completed (two issuers)
+  uint64_t epi_a;              // normalised O_lat (bf16) in q''s columns
+  uint64_t epi_done;           // output MMA done
+  uint64_t x_full[kXBuf];      // my receive buffer b holds the peer's partial S of a tile
+  uint64_t x_empty[kXBuf];     // the peer's receive buffer b may be used again
+  uint64_t x_consumed[kXBuf];  // my softmax threads are done with my receive buffer b
+  uint64_t epi_x;              // the peer's partial output of the item has arrived
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+constexpr int kQNumBars = 35;
+static_assert(offsetof(QBars, s_empty) == 10 * 8 && offsetof(QBars, p_full) == 12 * 8 &&
+                  offsetof(QBars, q_ready) == 18 * 8 && offsetof(QBars, o_last) == 19 * 8 &&
+                  offsetof(QBars, epi_a) == 20 * 8 && offsetof(QBars, x_consumed) == 30 * 8 &&
+                  offsetof(QBars, epi_x) == (kQNumBars - 1) * 8,
+              "pair persistent barrier indices");
+static_assert(sizeof(QBars) <= kBarBytes, "pair persistent barrier block");
+
+__device__ __forceinline__ uint32_t qbar_arrivals(int i) {
+  if (i == 10 || i == 11 || i == 18) return 384;     // s_empty, q_ready
+  if (i == 12 || i == 13 || i == 20) return 256;     // p_full, epi_a
+  if (i == 19) return 2;                             // o_last
+  if (i >= 30 && i <= 33) return 8;                  // x_consumed
+  return 1;
+}
+
+// The w_up_v slots of an item, s and s+1 (d = 128) or s alone: d chunk nc lives
+// at stage lo + nc * lbo / 32 KB (the lower stage first, whatever the slot order).
+__device__ __forceinline__ EpiStages wv_stages(int s, int dch) {
+  const uint32_t s0 = (uint32_t)(s % kStages), s1 = (uint32_t)((s + 1) % kStages);
+  EpiStages e;
+  e.wv_lo = dch > 1 ? min(s0, s1) : s0;
+  e.wv_lbo = dch > 1 ? (max(s0, s1) - min(s0, s1)) * (uint32_t)kLStage : (uint32_t)kLStage;
+  return e;
+}
+
+// The pair kernel's item of round r: the pair index and count are re-read from
+// the special registers at each call (cheap) instead of being kept live.
+__device__ __forceinline__ bool pair_item(const FlashArgs& a, int r, PItem& it) {
+  uint32_t cta, ncta;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(cta));
+  asm volatile("mov.u32 %0, %%nctaid.x;" : "=r"(ncta));
+  return persist_item(a, r, (int)(ncta >> 1), (int)(cta >> 1), it);
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+template <int kRC>
+__global__ void __launch_bounds__(kThreads, 1)
+    flash_persistent_pair_kernel(const __grid_constant__ CUtensorMap mapQ,
+                                 const __grid_constant__ CUtensorMap mapL,
+                                 const __grid_constant__ CUtensorMap mapWk,
+                                 const __grid_constant__ CUtensorMap mapWv, FlashArgs a) {
+  extern __shared__ uint8_t flash_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(flash_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sL = smem + kOffL;
+  uint8_t* sX = smem + kOffX;
+  QBars* bars = reinterpret_cast<QBars*>(smem + kOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+  constexpr int RC = kRC;
+  static_assert(RC * 128 <= kLStage, "weight slot");
+
+  grid_dep_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t peer = crank ^ 1u;
+  const int c0 = (int)crank * RC;                               // first rank column here
+  const int dch = a.d / 64;                                     // 64-column chunks of d
+  const int dh = a.d / 2;                                       // output columns stored here
+
+  if (warp == 0) {
+    uint64_t* const bar0 = &bars->l_full[0];
+    for (int i = lane; i < kQNumBars; i += 32) mbar_init(bar0 + i, qbar_arrivals(i));
+    if (lane == 0) bars->abort_flag = 0;
+    fence_mbarrier_init_cluster();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  const bool touches_peer = (warp >= 2 && warp < 6) || warp == 14;
+  cluster_arrive();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  grid_dep_wait();
+
+  if (warp == 0) {
+    // ======================= ring producer =======================
+    if (lane == 0) {
+      prefetch_tensormap(&mapL);
+      prefetch_tensormap(&mapWk);
+      prefetch_tensormap(&mapWv);
+      int S = 0, hi = 0;                   // next ring slot, slots issued
+      bool ok = true;
+      PItem it;
+      for (int r = 0; ok && pair_item(a, r, it); ++r) {
+        // w_up_k rows of this CTA's rank columns, one slot per 64 d columns
+        for (int kc = 0; ok && kc < dch; ++kc) {
+          const int slot = S + kc, st = slot % kStages;
+          if (!(ok = mbar_wait(&bars->l_empty[st], ((slot / kStages) & 1) ^ 1, 80, abort_flag)))
+            break;
+          mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(RC * 128));
+          tma_load_3d(sL + st * kLStage, &mapWk, &bars->l_full[st], 64 * kc, it.head, c0);
+          hi = slot + 1;
+        }
+        S += dch;
+        for (int j = 0; ok && j < it.nt; ++j) {
+          const int slot = S + j, st = slot % kStages;
+          if (!(ok = mbar_wait(&bars->l_empty[st], ((slot / kStages) & 1) ^ 1, 81, abort_flag)))
+            break;
+          mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(kKeys * RC * 2));
+          for (int kc = 0; kc < RC / 64; ++kc)
+            tma_load_3d(sL + st * kLStage + kc * (kKeys * 128), &mapL, &bars->l_full[st],
+                        c0 + 64 * kc, j * kKeys, it.b);
+          hi = slot + 1;
+        }
+        S += it.nt;
+        // w_up_v rows (MN-major B of the output MMA): both slots free first
+        for (int nc = 0; ok && nc < dch; ++nc) {
+          const int slot = S + nc;
+          ok = mbar_wait(&bars->l_empty[slot % kStages], ((slot / kStages) & 1) ^ 1, 82,
+                         abort_flag);
+        }
+        if (!ok) break;
+        const EpiStages ws = wv_stages(S, dch);
+        for (int nc = 0; nc < dch; ++nc) {
+          uint64_t* bar = &bars->l_full[(S + nc) % kStages];
+          mbar_arrive_expect_tx(bar, (uint32_t)(RC * 128));
+          for (int kb = 0; kb < RC / 64; ++kb)
+            tma_load_3d(sL + ws.wv_lo * kLStage + nc * ws.wv_lbo + kb * (64 * 128), &mapWv, bar,
+                        64 * nc, it.head, c0 + 64 * kb);
+        }
+        hi = S + dch;
+        S += dch;
+      }
+      if (!ok) {
+        // leave no copy in flight: the last slot of every stage (bounded waits)
+        for (int slot = max(0, hi - kStages); slot < hi; ++slot)
+          mbar_wait(&bars->l_full[slot % kStages], (slot / kStages) & 1, 83, nullptr);
+      }
+    }
+  } else if (warp == 1 || warp == 15) {
+    // ======================= MMA issuers =======================
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
+      constexpr uint32_t idesc_o = make_idesc_bf16(kRows, kRC, false, true);
+      constexpr uint32_t idesc_q = make_idesc_bf16(kRows, kRC, false, false);
+      const uint32_t idesc_v = make_idesc_bf16(kRows, a.d, false, true);
+      constexpr int kSSteps = kRC / 16;
+      const uint32_t l0 = smem_u32(sL), p0 = smem_u32(smem + kOffP), x0 = smem_u32(sX);
+      const uint32_t tq = tmem + kTmemQ;
+      // output MMA of an item: out_partial = O_lat(bf16, q''s columns) . w_up_v into
+      // S's columns, once the normalisation is done and the item's last two S tiles
+      // have been read
+      auto output_mma = [&](int r, int wv_slot, int t_end) -> bool {
+        bool good = mbar_wait(&bars->epi_a, r & 1, 84, abort_flag);
+        for (int g = max(t_end - 2, 0); good && g < t_end; ++g)
+          good = mbar_wait(&bars->s_empty[g & 1], (g >> 1) & 1, 85, abort_flag);
+        for (int nc = 0; good && nc < dch; ++nc) {
+          const int slot = wv_slot + nc;
+          good = mbar_wait(&bars->l_full[slot % kStages], (slot / kStages) & 1, 86, abort_flag);
+        }
+        if (!good) {
+          umma_commit(&bars->epi_done);
+          return false;
+        }
+        tc_fence_after();
+        const EpiStages ws = wv_stages(wv_slot, dch);
+        const uint64_t bv = make_sdesc_sw128(l0 + ws.wv_lo * kLStage, ws.wv_lbo, 1024);
+#pragma unroll
+        for (int k = 0; k < kRC / 16; ++k)
+          umma_bf16_ta(tmem + kTmemS, tq + k * 8, bv + (uint64_t)((k * 2048) >> 4), idesc_v,
+                       k > 0 ? 1u : 0u);
+        umma_commit(&bars->epi_done);
+        for (int nc = 0; nc < dch; ++nc) umma_commit(&bars->l_empty[(wv_slot + nc) % kStages]);
+        return true;
+      };
+      int T = 0, S = 0, r = 0, prev_wv = 0;
+      bool ok = true;
+      PItem it;
+      for (; ok && pair_item(a, r, it); ++r) {
+        const int wk_slot = S, l_slot = S + dch;
+        if (warp == 1) {
+          if (r > 0) ok = output_mma(r - 1, prev_wv, T);
+          // q' (fp32, this CTA's rank columns) = q . w_up_k^T into O's columns; A = the
+          // q tile in receive buffers T%4 and (T+1)%4, B = the w_up_k slots
+          ok = ok && mbar_wait(&bars->pro_full, r & 1, 87, abort_flag);
+          for (int kc = 0; ok && kc < dch; ++kc) {
+            const int slot = wk_slot + kc;
+            ok = mbar_wait(&bars->l_full[slot % kStages], (slot / kStages) & 1, 88, abort_flag);
+          }
+          if (ok) {
+            tc_fence_after();
+            for (int kc = 0; kc < dch; ++kc) {
+              const uint64_t aq = make_sdesc_sw128(x0 + (uint32_t)((T + kc) & 3) * kXBytes, 16, 1024);
+              const uint64_t bw =
+                  make_sdesc_sw128(l0 + (uint32_t)((wk_slot + kc) % kStages) * kLStage, 16, 1024);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                umma_bf16(tmem + kTmemO, aq + (uint64_t)((k * 32) >> 4),
+                          bw + (uint64_t)((k * 32) >> 4), idesc_q, (kc | k) ? 1u : 0u);
+            }
+          }
+          umma_commit(&bars->pro_done);
+          if (ok)
+            for (int kc = 0; kc < dch; ++kc) umma_commit(&bars->l_empty[(wk_slot + kc) % kStages]);
+        }
+        ok = ok && mbar_wait(&bars->q_ready, r & 1, 89, abort_flag);
+        tc_fence_after();
+        if (warp == 1) {
+          // S(g) = q' L(g)^T as soon as the tile has landed and S(g-2) has been read
+          for (int j = 0; ok && j < it.nt; ++j) {
+            const int g = T + j, slot = l_slot + j, st = slot % kStages;
+            ok = mbar_wait(&bars->l_full[st], (slot / kStages) & 1, 90, abort_flag) &&
+                 mbar_wait(&bars->s_empty[g & 1], ((g >> 1) & 1) ^ 1, 91, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t bds = make_sdesc_sw128(l0 + st * kLStage, 16, 1024);
+            const uint32_t sbuf = tmem + kTmemS + (g & 1) * kKeys;
+#pragma unroll
+            for (int k = 0; k < kSSteps; ++k)
+              umma_bf16_ta(sbuf, tq + k * 8,
+                           bds + (uint64_t)((((k) >> 2) * (kKeys * 128) + ((k) & 3) * 32) >> 4),
+                           idesc_s, k > 0 ? 1u : 0u);
+            umma_commit(&bars->s_full[g & 1]);
+          }
+        } else {
+          // O(g) += P(g) L(g), in tile order from this one thread
+          for (int j = 0; ok && j < it.nt; ++j) {
+            const int g = T + j, pb = g & 1, st = (l_slot + j) % kStages;
+            if (!(ok = mbar_wait(&bars->p_full[pb], (g >> 1) & 1, 92, abort_flag))) break;
+            tc_fence_after();
+            const uint64_t ad = make_sdesc_sw128(p0 + pb * kPBytes, 16, 1024);
+            const uint64_t bdo = make_sdesc_sw128(l0 + st * kLStage, kKeys * 128, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kKeys / 16; ++kk)   // the item's first product starts O
+              umma_bf16(tmem + kTmemO, ad + (uint64_t)((kk * 32) >> 4),
+                        bdo + (uint64_t)((kk * 2048) >> 4), idesc_o, (j | kk) ? 1u : 0u);
+            umma_commit(&bars->p_empty[pb]);
+            umma_commit(&bars->l_empty[st]);
+          }
+        }
+        umma_commit(&bars->o_last);
+        prev_wv = l_slot + it.nt;
+        T += it.nt;
+        S = l_slot + it.nt + dch;
+      }
+      if (warp == 1 && ok && r > 0) output_mma(r - 1, prev_wv, T);
+    }
+  } else if (warp < 6) {
+    // ======================= exchange with the peer =======================
+    cluster_wait();
+    const int qd = warp & 3;
+    const uint32_t rr = (uint32_t)(qd * 32 + lane);
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const uint32_t x_peer0 = mapa_shared(smem_u32(sX), peer);
+    const uint32_t xfull_peer0 = mapa_shared(smem_u32(&bars->x_full[0]), peer);
+    const uint32_t epx_peer = mapa_shared(smem_u32(&bars->epi_x), peer);
+    const int send0 = (int)peer * dh;      // output columns the peer stores
+    int T = 0;
+    uint32_t xpar = 0;                       // parity of each peer buffer's next release
+    bool ok = true;
+    PItem it;
+    for (int r = 0; ok; ++r) {
+      const bool have = pair_item(a, r, it);
+      // ---- boundary before item r: the previous item's output for the peer ----
+      float v[4][16];                      // dh <= 64 columns of my row
+      if (r > 0) {
+        if (!(ok = warp_wait(&bars->epi_done, (r - 1) & 1, 93, abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          if (c4 * 16 < dh) tmem_ld16(tmem + lane_base + kTmemS + send0 + c4 * 16, v[c4]);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      if (have) mbar_arrive(&bars->q_ready);   // item r's S may overwrite the output columns
+      if (r > 0) {
+        // fp16 rows scaled by a power of two (the row's largest magnitude in
+        // [2^14, 2^15)) into the peer's buffer (T+2)%4, the inverse factors into (T+3)%4
+        const int xa = (T + 2) & 3, xf = (T + 3) & 3;
+        if (!(ok = warp_wait<true>(&bars->x_empty[xa], (xpar >> xa) & 1u, 94, abort_flag) &&
+                   warp_wait<true>(&bars->x_empty[xf], (xpar >> xf) & 1u, 94, abort_flag)))
+          break;
+        xpar ^= (1u << xa) | (1u << xf);
+        const uint32_t xo = x_peer0 + (uint32_t)xa * kXBytes;
+        const uint32_t xs = x_peer0 + (uint32_t)xf * kXBytes;
+        float mx = 0.f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (c4 * 16 < dh) mx = fmaxf(mx, fabsf(v[c4][e]));
+        const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu);
+        const uint32_t sb = (uint32_t)min(max(268 - ex, 1), 253);
+        const float sc = __uint_as_float(sb << 23);
+        const float inv_sc = __uint_as_float((254u - sb) << 23);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            if (c4 * 16 < dh) {
+              const float* w = &v[c4][8 * h];
+              st_async_v4u(xo + xrow_offset(rr, (uint32_t)(2 * c4 + h), 128u),
+                           pack_half2(w[0] * sc, w[1] * sc), pack_half2(w[2] * sc, w[3] * sc),
+                           pack_half2(w[4] * sc, w[5] * sc), pack_half2(w[6] * sc, w[7] * sc),
+                           epx_peer);
+            }
+        st_async_v4u(xs + rr * 16, __float_as_uint(inv_sc), 0u, 0u, 0u, epx_peer);
+      }
+      if (!have) break;
+      // ---- the item's tiles: my partial S (fp16) into the peer's buffer g%4 ----
+      for (int j = 0; j < it.nt; ++j) {
+        const int g = T + j, bi = g & 1, k = g >> 1, xb = g & 3;
+        if (!warp_wait<true>(&bars->x_empty[xb], (xpar >> xb) & 1u, 95, abort_flag) ||
+            !warp_wait(&bars->s_full[bi], k & 1, 96, abort_flag)) {
+          ok = false;
+          break;
+        }
+        xpar ^= 1u << xb;
+        tc_fence_after();
+        const uint32_t dst = x_peer0 + xb * kXBytes;
+        const uint32_t bar = xfull_peer0 + xb * 8;
+        float s2[2][32];
+        tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys, s2[0]);
+        tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys + 32, s2[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_empty[bi]);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            st_async_v4u(dst + sw128_offset(rr, hh * 4 + c),
+                         pack_half2(s2[hh][8 * c], s2[hh][8 * c + 1]),
+                         pack_half2(s2[hh][8 * c + 2], s2[hh][8 * c + 3]),
+                         pack_half2(s2[hh][8 * c + 4], s2[hh][8 * c + 5]),
+                         pack_half2(s2[hh][8 * c + 6], s2[hh][8 * c + 7]), bar);
+      }
+      T += it.nt;
+    }
+  } else if (warp == 14) {
+    // ======================= releases and q tiles =======================
+    // Consumption events of item r, in order, at positions p = -4..nt-1 of
+    // buffer (T+p)%4: p = -4, -3 the absorption has read the item's q tile;
+    // p = -2, -1 the previous item's partial output has been stored (item 0:
+    // the initial release); p >= 0 tile T+p.  Each is forwarded to the peer,
+    // except the last uses of the next item's q buffers (p = nt-4, nt-3).
+    cluster_wait();
+    if (lane == 0) {
+      prefetch_tensormap(&mapQ);
+      const uint32_t xe_peer0 = mapa_shared(smem_u32(&bars->x_empty[0]), peer);
+      // the q tile of an item starting at global tile t0 into buffers t0%4, (t0+1)%4
+      auto load_q = [&](const PItem& q_it, int t0) {
+        mbar_arrive_expect_tx(&bars->pro_full, (uint32_t)(kRows * a.d * 2));
+        for (int kc = 0; kc < dch; ++kc)
+          tma_load_3d(sX + ((t0 + kc) & 3) * kXBytes, &mapQ, &bars->pro_full, 64 * kc, q_it.head,
+                      q_it.b * a.Tq + q_it.row0);
+      };
+      bool ok = true;
+      uint32_t cpar = 0;                   // parity of each buffer's next consumption
+      PItem it, nx;
+      int T = 0, armed = -1;
+      if (pair_item(a, 0, it)) {
+        load_q(it, 0);
+        armed = 0;
+      }
+      for (int r = 0; ok && pair_item(a, r, it); ++r) {
+        const bool have_next = pair_item(a, r + 1, nx);
+        for (int p = -4; p < it.nt; ++p) {
+          const int xb = (T + p) & 3;
+          if (!(ok = mbar_wait(&bars->x_consumed[xb], (cpar >> xb) & 1u, 97, abort_flag))) break;
+          cpar ^= 1u << xb;
+          if (!(have_next && (p == it.nt - 4 || p == it.nt - 3)))
+            mbar_arrive_remote(xe_peer0 + (uint32_t)xb * 8);
+          if (have_next && p == it.nt - 3) {   // both of the next q buffers are free
+            load_q(nx, T + it.nt);
+            armed = r + 1;
+          }
+        }
+        T += it.nt;
+      }
+      if (!ok && armed >= 0) mbar_wait(&bars->pro_full, armed & 1, 98, nullptr);
+    }
+  } else if (warp >= 6) {
+    // ======================= softmax, conversions, stores =======================
+    const int qd = warp & 3;
+    const int half = (warp - 6) >> 2;
+    const int r_ = qd * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const uint32_t x_local = smem_u32(sX);
+    const uint32_t red_mine = smem_u32(smem + kOffRed) + (uint32_t)(half * 128 + r_) * 4;
+    const uint32_t red_other = red_mine ^ (128u * 4u);      // the partner warp's slot
+    const uint32_t bar_id = 1u + (uint32_t)qd;
+    const int oc0 = half * (RC / 2);
+    const int nq = dh / 2;                                   // output columns of this warp
+    if (warp == 6 && lane == 0) {
+      // receive barriers of the first four tiles and of item 0's partial output
+      for (int xb = 0; xb < kXBuf; ++xb)
+        mbar_arrive_expect_tx(&bars->x_full[xb], (uint32_t)kXBytes);
+      mbar_arrive_expect_tx(&bars->epi_x, epi_x_bytes(dh));
+    }
+    __syncwarp();
+    if (lane == 0) {                       // initial release of buffers 2 and 3 (0 and 1
+      mbar_arrive(&bars->x_consumed[2]);   // hold item 0's q tile)
+      mbar_arrive(&bars->x_consumed[3]);
+    }
+    int T = 0;
+    bool ok = true;
+    PItem it;
+    for (int r = 0; ok; ++r) {
+      const bool have = pair_item(a, r, it);
+      // ---- boundary: item r's q' into TMEM, item r-1's output out ----
+      if (have) {
+        if (!(ok = warp_wait(&bars->pro_done, r & 1, 99, abort_flag))) break;
+        tc_fence_after();
+        tmem_rows_to_bf16(tmem + lane_base + kTmemO + oc0, tmem + lane_base + kTmemQ + oc0 / 2,
+                          RC / 2, a.qscale);
+      }
+      float ov[2][16];
+      // first output column of this warp (re-read here, not kept across the tiles)
+      const int cfirst = (int)cluster_ctarank() * dh + half * nq;
+      if (r > 0) {
+        if (!(ok = warp_wait(&bars->epi_done, (r - 1) & 1, 100, abort_flag))) break;
+        tc_fence_after();
+        tmem_ld16(tmem + lane_base + kTmemS + cfirst, ov[0]);
+        if (nq > 16) tmem_ld16(tmem + lane_base + kTmemS + cfirst + 16, ov[1]);
+        tmem_wait_ld();
+      }
+      if (have) {
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->q_ready);
+        __syncwarp();
+        if (lane == 0) {                     // the absorption has read the q buffers
+          mbar_arrive(&bars->x_consumed[T & 3]);
+          mbar_arrive(&bars->x_consumed[(T + 1) & 3]);
+        }
+      }
+      if (r > 0) {
+        // the peer's partial product for my columns, fp16 rows times 2^k
+        if (!(ok = warp_wait<true>(&bars->epi_x, (r - 1) & 1, 101, abort_flag))) break;
+        const uint32_t xo = x_local + (uint32_t)((T + 2) & 3) * kXBytes;
+        const uint32_t xs = x_local + (uint32_t)((T + 3) & 3) * kXBytes;
+        float inv_sc, y0, y1, y2;
+        ld_shared_v4f(xs + (uint32_t)r_ * 16, inv_sc, y0, y1, y2);
+        const int cc0 = half * nq;            // first column within the received half
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {         // 8 fp16 per 16-byte chunk
+          if (q * 8 < nq) {
+            float x[4];
+            ld_shared_v4f(xo + xrow_offset((uint32_t)r_, (uint32_t)((cc0 >> 3) + q), 128u), x[0],
+                          x[1], x[2], x[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = unpack_half2(__float_as_uint(x[e]));
+              ov[q >> 1][8 * (q & 1) + 2 * e] += f.x * inv_sc;
+              ov[q >> 1][8 * (q & 1) + 2 * e + 1] += f.y * inv_sc;
+            }
+          }
+        }
+        if (have && warp == 6 && lane == 0)  // item r's partial output comes next
+          mbar_arrive_expect_tx(&bars->epi_x, epi_x_bytes(dh));
+        __syncwarp();
+        if (have && lane == 0) {             // the partial-output buffers are free
+          mbar_arrive(&bars->x_consumed[(T + 2) & 3]);
+          mbar_arrive(&bars->x_consumed[(T + 3) & 3]);
+        }
+        PItem prev;
+        pair_item(a, r - 1, prev);
+        const int pgrow = prev.row0 + r_;
+        if (pgrow < a.Tq) {
+          const int64_t orow = (((int64_t)prev.b * a.Tq + pgrow) * a.H + prev.head) * a.d + cfirst;
+          if (a.out_bf16) {
+            uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (q * 8 < nq) {
+                const float* w = &ov[q >> 1][8 * (q & 1)];
+                d4[q] = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                                   pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+              }
+          } else {
+            float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (q * 4 < nq) {
+                const float* w = &ov[q >> 2][4 * (q & 3)];
+                d4[q] = make_float4(w[0], w[1], w[2], w[3]);
+              }
+          }
+        }
+      }
+      if (!have) break;
+
+      // ---- the item's tiles ----
+      // keys visible to my row: key < lim (none for a row past the end)
+      const int grow = it.row0 + r_;
+      const int lim = grow >= a.Tq ? 0 : a.causal ? min(a.Tkv - a.Tq + grow + 1, a.Tkv) : a.Tkv;
+      const int key_base = half * 32 - T * kKeys;     // key0 of tile g = g * 64 + key_base
+      const int g_end = T + it.nt;
+      float m_run = -INFINITY, l_half = 0.f;
+      for (int g = T; g < g_end; ++g) {
+        const int bi = g & 1, k = g >> 1, xb = g & 3;
+        float s[32];
+        if (!(ok = warp_wait(&bars->s_full[bi], k & 1, 102, abort_flag))) break;
+        tc_fence_after();
+        tmem_ld32(tmem + lane_base + kTmemS + bi * kKeys + half * 32, s);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_empty[bi]);
+        // the peer's partial S over its half of the rank (my 32 keys)
+        if (!(ok = warp_wait<true>(&bars->x_full[xb], (g >> 2) & 1, 103, abort_flag))) break;
+        const uint32_t src = x_local + xb * kXBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u0, u1, u2, u3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(u0), "=r"(u1), "=r"(u2), "=r"(u3)
+                       : "r"(src + sw128_offset((uint32_t)r_, (uint32_t)(half * 4 + c)))
+                       : "memory");
+          const float2 f[4] = {unpack_half2(u0), unpack_half2(u1), unpack_half2(u2),
+                               unpack_half2(u3)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 t = __fadd2_rn(make_float2(s[8 * c + 2 * e], s[8 * c + 2 * e + 1]), f[e]);
+            s[8 * c + 2 * e] = t.x;
+            s[8 * c + 2 * e + 1] = t.y;
+          }
+        }
+        if (warp == 6 && lane == 0)          // this buffer's next tile
+          mbar_arrive_expect_tx(&bars->x_full[xb], (uint32_t)kXBytes);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->x_consumed[xb]);
+
+        const int key0 = g * kKeys + key_base;
+        if (key0 + 32 > lim) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (key0 + c >= lim) s[c] = -INFINITY;
+        }
+        const float mx_half = tree_max32(s);
+        st_shared_f32(red_mine, mx_half);
+        named_bar_sync(bar_id, 64);
+        const float mx = fmaxf(mx_half, ld_shared_f32(red_other));
+        named_bar_sync(bar_id, 64);
+        const float m_new = fmaxf(m_run, mx);
+        const bool grow_max = m_new > m_run + kRescaleThreshold;
+        const float m_ref = grow_max ? m_new : m_run;
+        const float alpha = grow_max ? ex2(m_run - m_new) : 1.f;
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float2 t = __fadd2_rn(make_float2(s[2 * c], s[2 * c + 1]),
+                                      make_float2(-m_use, -m_use));
+          s[2 * c] = ex2(t.x);
+          s[2 * c + 1] = ex2(t.y);
+        }
+        l_half = l_half * alpha + tree_sum32(s);
+        m_run = m_ref;
+        if (!(ok = warp_wait(&bars->p_empty[bi], (k & 1) ^ 1, 104, abort_flag))) break;
+        if (__any_sync(0xffffffffu, grow_max && g > T)) {
+          if (!(ok = warp_wait(&bars->p_empty[(g - 1) & 1], ((g - 1) >> 1) & 1, 105, abort_flag)))
+            break;
+          tc_fence_after();
+          for (int c = oc0; c < oc0 + RC / 2; c += 16) {
+            float o[16];
+            tmem_ld16(tmem + lane_base + kTmemO + c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float2 t = __fmul2_rn(make_float2(o[2 * e], o[2 * e + 1]),
+                                          make_float2(alpha, alpha));
+              o[2 * e] = t.x;
+              o[2 * e + 1] = t.y;
+            }
+            tmem_st16(tmem + lane_base + kTmemO + c, o);
+          }
+          tmem_wait_st();
+        }
+        const uint32_t pb = smem_u32(smem + kOffP + bi * kPBytes);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          st_shared_v4(pb + sw128_offset(r_, half * 4 + c), pack_bf16x2(s[8 * c], s[8 * c + 1]),
+                       pack_bf16x2(s[8 * c + 2], s[8 * c + 3]),
+                       pack_bf16x2(s[8 * c + 4], s[8 * c + 5]),
+                       pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[bi]);
+      }
+      if (!ok) break;
+
+      // ---- end of the item: normalised O_lat (bf16) into q''s columns ----
+      // the row sum is the two halves' sums, added in the same order in both warps
+      st_shared_f32(red_mine, l_half);
+      named_bar_sync(bar_id, 64);
+      const float l_lo = ld_shared_f32(half ? red_other : red_mine);
+      const float l_hi = ld_shared_f32(half ? red_mine : red_other);
+      const float l_run = l_lo + l_hi;
+      named_bar_sync(bar_id, 64);
+      if (!(ok = warp_wait(&bars->o_last, r & 1, 106, abort_flag))) break;
+      tc_fence_after();
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      tmem_rows_to_bf16(tmem + lane_base + kTmemO + oc0, tmem + lane_base + kTmemQ + oc0 / 2,
+                        RC / 2, inv);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->epi_a);
+      T += it.nt;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (!touches_peer) cluster_wait();
+  cluster_sync();     // neither CTA leaves while the other may still address it
 }
 
 // ---------------------------------------------------------------------------
@@ -1559,6 +2238,92 @@ cudaError_t launch_flash_persistent(const CUtensorMap& mapQ, const CUtensorMap& 
     case 128: return launch_persistent_rc<128>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
     case 192: return launch_persistent_rc<192>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
     case 256: return launch_persistent_rc<256>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int kRC>
+static cudaLaunchConfig_t pair_config(int pairs, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+// CTA pairs of the persistent pair kernel that fit on the current device at
+// once (a cluster needs two free SMs of one GPC), 0 if the query fails.
+template <int kRC>
+static int pair_slots_rc() {
+  auto kern = flash_persistent_pair_kernel<kRC>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pair_config<kRC>(1, nullptr, attr);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return clusters;
+}
+
+int flash_pair_slots(int RC) {
+  constexpr int kDevices = 64;
+  static std::atomic<int> cache[2][kDevices];   // 0: not yet queried, else slots + 1
+  if (RC != 192 && RC != 256) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::atomic<int>& c = cache[RC == 256 ? 1 : 0][dev];
+  int v = c.load(std::memory_order_relaxed);
+  if (v == 0) {
+    v = (RC == 256 ? pair_slots_rc<256>() : pair_slots_rc<192>()) + 1;
+    c.store(v, std::memory_order_relaxed);
+  }
+  return v - 1;
+}
+
+template <int kRC>
+static cudaError_t launch_persistent_pair_rc(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                             const CUtensorMap& mapWk, const CUtensorMap& mapWv,
+                                             const FlashArgs& args, int pairs,
+                                             cudaStream_t stream) {
+  auto kern = flash_persistent_pair_kernel<kRC>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pair_config<kRC>(pairs, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flash_persistent_pair(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                         const CUtensorMap& mapWk, const CUtensorMap& mapWv,
+                                         const FlashArgs& args, int pairs, cudaStream_t stream) {
+  if (!args.pair || (args.d != 64 && args.d != 128) || args.cu_q != nullptr || pairs <= 0)
+    return cudaErrorInvalidValue;
+  switch (args.RC) {
+    case 192:
+      return launch_persistent_pair_rc<192>(mapQ, mapL, mapWk, mapWv, args, pairs, stream);
+    case 256:
+      return launch_persistent_pair_rc<256>(mapQ, mapL, mapWk, mapWv, args, pairs, stream);
     default: return cudaErrorInvalidValue;
   }
 }

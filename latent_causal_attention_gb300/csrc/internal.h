@@ -93,6 +93,16 @@ cudaError_t launch_flash_persistent(const CUtensorMap& mapQ, const CUtensorMap& 
                                     const CUtensorMap& mapWk, const CUtensorMap& mapWv,
                                     const FlashArgs& args, int num_ctas, cudaStream_t stream);
 
+// Persistent CTA-pair prefill (rank 384 or 512, d = 64 or 128, dense batch):
+// `pairs` resident clusters of two CTAs (at most flash_pair_slots(RC)) work
+// through the items; maps as launch_flash_persistent; results bitwise equal to
+// launch_flash_fused's.  flash_pair_slots returns how many such pairs fit on
+// the current device at once (cached per device), 0 when unknown.
+int flash_pair_slots(int RC);
+cudaError_t launch_flash_persistent_pair(const CUtensorMap& mapQ, const CUtensorMap& mapL,
+                                         const CUtensorMap& mapWk, const CUtensorMap& mapWv,
+                                         const FlashArgs& args, int pairs, cudaStream_t stream);
+
 cudaError_t launch_merge_partials(const float* m_l, int ml_stride, const float* l, const float* o,
                                   void* out, int parts, int rows, int width, int out_bf16,
                                   cudaStream_t stream);

@@ -396,15 +396,28 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
     fa.row_blocks = p.row_blocks; fa.splits = 1; fa.causal = causal ? 1 : 0;
     fa.d = d; fa.qscale = scale * 1.4426950408889634f; fa.out = out;
     fa.out_bf16 = out_dtype == MLA_BF16;
+    const int64_t items = (int64_t)p.row_blocks * B * H;
     if (g_persistent && !p.pair && d == 64) {
       // one resident CTA per SM works through the (b, head, row block) items
-      const int64_t items = (int64_t)p.row_blocks * B * H;
       const int ctas = (int)(items < planner_sm_count() ? items : planner_sm_count());
       if (staged(1, stream, [&] {
             return launch_flash_persistent(mQ, mL, mWk, mWv, fa, ctas, stream);
           }) != cudaSuccess)
         return MLA_ERR_CUDA;
       return MLA_OK;
+    }
+    if (g_persistent && p.pair) {
+      // one resident CTA pair per two SMs (as many as fit at once)
+      int64_t pairs = flash_pair_slots(p.RC);
+      if (pairs > planner_sm_count() / 2) pairs = planner_sm_count() / 2;
+      if (pairs > items) pairs = items;
+      if (pairs > 0) {
+        if (staged(1, stream, [&] {
+              return launch_flash_persistent_pair(mQ, mL, mWk, mWv, fa, (int)pairs, stream);
+            }) != cudaSuccess)
+          return MLA_ERR_CUDA;
+        return MLA_OK;
+      }
     }
     if (staged(1, stream,
                [&] { return launch_flash_fused(mQ, mL, mWk, mWv, mO, fa, stream); }) !=

@@ -532,20 +532,29 @@ def test_calls_capture_into_a_cuda_graph():
     assert mla.device_error() == 0
 
 
-# ------------------------------------------- persistent single-CTA prefill
+# ------------------------------------------- persistent prefill (single CTA and CTA pair)
 PERSIST = [
     dict(B=2, Tq=300, Tkv=300, H=4, d=64, rank=256, causal=True),     # ragged row blocks
     dict(B=1, Tq=200, Tkv=700, H=3, d=64, rank=128, causal=True),     # chunked prefill
     dict(B=3, Tq=128, Tkv=128, H=2, d=64, rank=64, causal=False),     # no mask
     dict(B=1, Tq=1024, Tkv=1024, H=40, d=64, rank=192, causal=True),  # 320 items: several rounds
+    # CTA pairs (rank > 256): items of one to five tiles, so that every receive
+    # buffer takes q tiles and partial outputs in turn
+    dict(B=2, Tq=300, Tkv=300, H=3, d=128, rank=512, causal=True),    # ragged, 2..5 tiles
+    dict(B=1, Tq=200, Tkv=700, H=2, d=64, rank=384, causal=True),     # chunked, d 64, RC 192
+    dict(B=3, Tq=64, Tkv=64, H=2, d=128, rank=512, causal=True),      # one-tile items
+    dict(B=2, Tq=130, Tkv=130, H=2, d=128, rank=512, causal=False),   # no mask, 3-tile items
+    dict(B=1, Tq=1024, Tkv=1024, H=40, d=128, rank=512, causal=True), # 320 items: several rounds
+    dict(B=1, Tq=640, Tkv=640, H=36, d=64, rank=384, causal=True),    # 180 items, RC 192
 ]
 
 
 @pytest.mark.parametrize("shape", PERSIST, ids=lambda s: "x".join(str(v) for v in s.values()))
 def test_persistent_prefill_matches_per_block_kernel(oracle, shape):
-    """Long prefill with rank <= 256 and d = 64 runs one resident CTA per SM
-    over all row blocks; it does the same arithmetic as one CTA per row block,
-    so the two agree bit for bit, and both match the oracle."""
+    """Long prefill runs resident CTAs (rank <= 256, d = 64) or resident CTA
+    pairs (rank 384 / 512) over all row blocks; they do the same arithmetic as
+    one CTA (pair) per row block, so the two agree bit for bit, and both match
+    the oracle."""
     w = custom_workload("persist", dtype="bf16", **shape)
     x = make_inputs(w, seed=13)
     outs = {}
