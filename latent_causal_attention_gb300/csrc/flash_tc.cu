@@ -1433,10 +1433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // waits until the absorption has read the q tile.
 //
 // Roles: warp 0 lane 0 ring producer; warp 1 lane 0 absorption, S MMAs and
-// output MMA; warp 15 lane 0 O MMAs; warps 2-5 partial-S exchange and the
-// partial-output send; warp 14 lane 0 release forwarding and the q-tile loads
-// (it sees every consumption of the receive buffers in order); warps 6-13
-// softmax, normalisation, the q' conversion and the stores.
+// output MMA; warp 15 lane 0 O MMAs; warps 2-5 partial-S exchange and, at an
+// item boundary, the output: the peer's half sent, this CTA's half added to
+// the peer's partial and stored (tile stores staged in the P buffers, which
+// the softmax threads write again only after stg_free); warp 14 lane 0
+// release forwarding and the q-tile loads (it sees every consumption of the
+// receive buffers in order); warps 6-13 softmax, normalisation and the q'
+// conversion.
 // ---------------------------------------------------------------------------
 struct QBars {
   uint64_t l_full[kStages];    // ring slot landed (latent tile, w_up_k or w_up_v rows)
@@ -1455,14 +1458,15 @@ struct QBars {
   uint64_t x_empty[kXBuf];     // the peer's receive buffer b may be used again
   uint64_t x_consumed[kXBuf];  // my softmax threads are done with my receive buffer b
   uint64_t epi_x;              // the peer's partial output of the item has arrived
+  uint64_t stg_free;           // the item's output staging (P buffers) has been read out
   uint32_t tmem_slot;
   int abort_flag;
 };
-constexpr int kQNumBars = 35;
+constexpr int kQNumBars = 36;
 static_assert(offsetof(QBars, s_empty) == 10 * 8 && offsetof(QBars, p_full) == 12 * 8 &&
                   offsetof(QBars, q_ready) == 18 * 8 && offsetof(QBars, o_last) == 19 * 8 &&
                   offsetof(QBars, epi_a) == 20 * 8 && offsetof(QBars, x_consumed) == 30 * 8 &&
-                  offsetof(QBars, epi_x) == (kQNumBars - 1) * 8,
+                  offsetof(QBars, epi_x) == 34 * 8 && offsetof(QBars, stg_free) == 35 * 8,
               "pair persistent barrier indices");
 static_assert(sizeof(QBars) <= kBarBytes, "pair persistent barrier block");
 
@@ -1502,12 +1506,13 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   return v;
 }
 
-template <int kRC>
+template <int kRC, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_persistent_pair_kernel(const __grid_constant__ CUtensorMap mapQ,
                                  const __grid_constant__ CUtensorMap mapL,
                                  const __grid_constant__ CUtensorMap mapWk,
-                                 const __grid_constant__ CUtensorMap mapWv, FlashArgs a) {
+                                 const __grid_constant__ CUtensorMap mapWv,
+                                 const __grid_constant__ CUtensorMap mapO, FlashArgs a) {
   extern __shared__ uint8_t flash_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(flash_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1523,8 +1528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t crank = cluster_ctarank();
   const uint32_t peer = crank ^ 1u;
   const int c0 = (int)crank * RC;                               // first rank column here
-  const int dch = a.d / 64;                                     // 64-column chunks of d
-  const int dh = a.d / 2;                                       // output columns stored here
+  constexpr int dch = kD / 64;                                 // 64-column chunks of d
+  constexpr int dh = kD / 2;                                   // output columns stored here
 
   if (warp == 0) {
     uint64_t* const bar0 = &bars->l_full[0];
@@ -1602,7 +1607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = make_idesc_bf16(kRows, kKeys, false, false);
       constexpr uint32_t idesc_o = make_idesc_bf16(kRows, kRC, false, true);
       constexpr uint32_t idesc_q = make_idesc_bf16(kRows, kRC, false, false);
-      const uint32_t idesc_v = make_idesc_bf16(kRows, a.d, false, true);
+      constexpr uint32_t idesc_v = make_idesc_bf16(kRows, kD, false, true);
       constexpr int kSSteps = kRC / 16;
       const uint32_t l0 = smem_u32(sL), p0 = smem_u32(smem + kOffP), x0 = smem_u32(sX);
       const uint32_t tq = tmem + kTmemQ;
@@ -1714,56 +1719,149 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t xfull_peer0 = mapa_shared(smem_u32(&bars->x_full[0]), peer);
     const uint32_t epx_peer = mapa_shared(smem_u32(&bars->epi_x), peer);
     const int send0 = (int)peer * dh;      // output columns the peer stores
+    const uint32_t x_local = smem_u32(sX);
     int T = 0;
     uint32_t xpar = 0;                       // parity of each peer buffer's next release
     bool ok = true;
     PItem it;
+    if (warp == 2 && lane == 0)            // item 0's partial output from the peer
+      mbar_arrive_expect_tx(&bars->epi_x, epi_x_bytes(dh));
     for (int r = 0; ok; ++r) {
       const bool have = pair_item(a, r, it);
-      // ---- boundary before item r: the previous item's output for the peer ----
-      float v[4][16];                      // dh <= 64 columns of my row
+      // ---- boundary before item r: the previous item's output ----
       if (r > 0) {
+        float v[4][16];                    // dh <= 64 columns of my row
         if (!(ok = warp_wait(&bars->epi_done, (r - 1) & 1, 93, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4)
           if (c4 * 16 < dh) tmem_ld16(tmem + lane_base + kTmemS + send0 + c4 * 16, v[c4]);
         tmem_wait_ld();
-      }
-      tc_fence_before();
-      if (have) mbar_arrive(&bars->q_ready);   // item r's S may overwrite the output columns
-      if (r > 0) {
-        // fp16 rows scaled by a power of two (the row's largest magnitude in
-        // [2^14, 2^15)) into the peer's buffer (T+2)%4, the inverse factors into (T+3)%4
+        // the peer's half: fp16 rows scaled by a power of two (the row's largest
+        // magnitude in [2^14, 2^15)) into the peer's buffer (T+2)%4, the inverse
+        // factors into (T+3)%4
         const int xa = (T + 2) & 3, xf = (T + 3) & 3;
         if (!(ok = warp_wait<true>(&bars->x_empty[xa], (xpar >> xa) & 1u, 94, abort_flag) &&
                    warp_wait<true>(&bars->x_empty[xf], (xpar >> xf) & 1u, 94, abort_flag)))
           break;
         xpar ^= (1u << xa) | (1u << xf);
-        const uint32_t xo = x_peer0 + (uint32_t)xa * kXBytes;
-        const uint32_t xs = x_peer0 + (uint32_t)xf * kXBytes;
-        float mx = 0.f;
+        {
+          const uint32_t xo = x_peer0 + (uint32_t)xa * kXBytes;
+          const uint32_t xs = x_peer0 + (uint32_t)xf * kXBytes;
+          float mx = 0.f;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (c4 * 16 < dh) mx = fmaxf(mx, fabsf(v[c4][e]));
+          const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu);
+          const uint32_t sb = (uint32_t)min(max(268 - ex, 1), 253);
+          const float sc = __uint_as_float(sb << 23);
+          const float inv_sc = __uint_as_float((254u - sb) << 23);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              if (c4 * 16 < dh) {
+                const float* w = &v[c4][8 * h];
+                st_async_v4u(xo + xrow_offset(rr, (uint32_t)(2 * c4 + h), 128u),
+                             pack_half2(w[0] * sc, w[1] * sc), pack_half2(w[2] * sc, w[3] * sc),
+                             pack_half2(w[4] * sc, w[5] * sc), pack_half2(w[6] * sc, w[7] * sc),
+                             epx_peer);
+              }
+          st_async_v4u(xs + rr * 16, __float_as_uint(inv_sc), 0u, 0u, 0u, epx_peer);
+        }
+        // my half, then item r's S may overwrite the output columns
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4)
+          if (c4 * 16 < dh)
+            tmem_ld16(tmem + lane_base + kTmemS + (int)crank * dh + c4 * 16, v[c4]);
+        tmem_wait_ld();
+        tc_fence_before();
+        if (have) mbar_arrive(&bars->q_ready);
+        // plus the peer's partial product for my half (fp16 rows times 2^k)
+        if (!(ok = warp_wait<true>(&bars->epi_x, (r - 1) & 1, 101, abort_flag))) break;
+        {
+          const uint32_t xo = x_local + (uint32_t)((T + 2) & 3) * kXBytes;
+          const uint32_t xs = x_local + (uint32_t)((T + 3) & 3) * kXBytes;
+          float inv_sc, y0, y1, y2;
+          ld_shared_v4f(xs + rr * 16, inv_sc, y0, y1, y2);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            if (c4 * 16 < dh) mx = fmaxf(mx, fabsf(v[c4][e]));
-        const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu);
-        const uint32_t sb = (uint32_t)min(max(268 - ex, 1), 253);
-        const float sc = __uint_as_float(sb << 23);
-        const float inv_sc = __uint_as_float((254u - sb) << 23);
+          for (int q = 0; q < 8; ++q) {          // 8 fp16 per 16-byte chunk
+            if (q * 8 < dh) {
+              float x[4];
+              ld_shared_v4f(xo + xrow_offset(rr, (uint32_t)q, 128u), x[0], x[1], x[2], x[3]);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            if (c4 * 16 < dh) {
-              const float* w = &v[c4][8 * h];
-              st_async_v4u(xo + xrow_offset(rr, (uint32_t)(2 * c4 + h), 128u),
-                           pack_half2(w[0] * sc, w[1] * sc), pack_half2(w[2] * sc, w[3] * sc),
-                           pack_half2(w[4] * sc, w[5] * sc), pack_half2(w[6] * sc, w[7] * sc),
-                           epx_peer);
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_half2(__float_as_uint(x[e]));
+                v[q >> 1][8 * (q & 1) + 2 * e] += f.x * inv_sc;
+                v[q >> 1][8 * (q & 1) + 2 * e + 1] += f.y * inv_sc;
+              }
             }
-        st_async_v4u(xs + rr * 16, __float_as_uint(inv_sc), 0u, 0u, 0u, epx_peer);
+            if (q == 3) asm volatile("" ::: "memory");   // two halves: fewer loads in flight
+          }
+        }
+        if (have && warp == 2 && lane == 0)  // item r's partial output comes next
+          mbar_arrive_expect_tx(&bars->epi_x, epi_x_bytes(dh));
+        __syncwarp();
+        if (have && lane < 2) {              // the partial-output buffers are free
+          mbar_arrive(&bars->x_consumed[(T + 2) & 3]);
+          mbar_arrive(&bars->x_consumed[(T + 3) & 3]);
+        }
+        // out[b, i, h, crank*dh ..+dh) by tile stores of 128 x 128-byte boxes staged
+        // (128-byte swizzle) in the P buffers, free between the item's last O MMA and
+        // the next item's first P; the map is per batch entry, so the rows of a
+        // partial block past the sequence's end are not written.  (bf16 with d = 64
+        // stores 64 bytes per row: row by row.)
+        PItem prev;
+        pair_item(a, r - 1, prev);
+        constexpr bool kBoxesFit = dh % 64 == 0;   // both dtypes' boxes tile the columns
+        if (kBoxesFit || !a.out_bf16) {
+          const uint32_t stg = smem_u32(smem + kOffP);
+          const uint32_t row = stg + rr * 128, sw = rr & 7;
+          if (a.out_bf16) {
+#pragma unroll
+            for (int q = 0; q < dh / 8; ++q) {
+              const float* w = &v[q >> 1][8 * (q & 1)];
+              st_shared_v4(row + (uint32_t)(q >> 3) * (kRows * 128) + ((((uint32_t)q & 7u) ^ sw) << 4),
+                           pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                           pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < dh / 4; ++q) {
+              const float* w = &v[q >> 2][4 * (q & 3)];
+              st_shared_v4(row + (uint32_t)(q >> 3) * (kRows * 128) + ((((uint32_t)q & 7u) ^ sw) << 4),
+                           __float_as_uint(w[0]), __float_as_uint(w[1]), __float_as_uint(w[2]),
+                           __float_as_uint(w[3]));
+            }
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(6, 128);                  // all four warps have staged their rows
+          if (warp == 2 && lane == 0) {
+            const int box_cols = a.out_bf16 ? 64 : 32;
+            for (int bx = 0; bx < dh / box_cols; ++bx)
+              tma_store_4d(&mapO, stg + (uint32_t)bx * (kRows * 128),
+                           (int)crank * dh + bx * box_cols, prev.head, prev.row0, prev.b);
+            bulk_commit_group();
+            bulk_wait_read_all();                  // the staging must outlive the reads
+          }
+        } else if (prev.row0 + (int)rr < a.Tq) {
+          const int64_t orow =
+              (((int64_t)prev.b * a.Tq + prev.row0 + (int)rr) * a.H + prev.head) * kD +
+              (int)crank * dh;
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
+#pragma unroll
+          for (int q = 0; q < dh / 8; ++q) {
+            const float* w = &v[q >> 1][8 * (q & 1)];
+            d4[q] = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                               pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+          }
+        }
+        if (warp == 2 && lane == 0) mbar_arrive(&bars->stg_free);
+      } else {
+        tc_fence_before();
+        mbar_arrive(&bars->q_ready);
       }
       if (!have) break;
       // ---- the item's tiles: my partial S (fp16) into the peer's buffer g%4 ----
@@ -1809,7 +1907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t xe_peer0 = mapa_shared(smem_u32(&bars->x_empty[0]), peer);
       // the q tile of an item starting at global tile t0 into buffers t0%4, (t0+1)%4
       auto load_q = [&](const PItem& q_it, int t0) {
-        mbar_arrive_expect_tx(&bars->pro_full, (uint32_t)(kRows * a.d * 2));
+        mbar_arrive_expect_tx(&bars->pro_full, (uint32_t)(kRows * kD * 2));
         for (int kc = 0; kc < dch; ++kc)
           tma_load_3d(sX + ((t0 + kc) & 3) * kXBytes, &mapQ, &bars->pro_full, 64 * kc, q_it.head,
                       q_it.b * a.Tq + q_it.row0);
@@ -1840,7 +1938,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && armed >= 0) mbar_wait(&bars->pro_full, armed & 1, 98, nullptr);
     }
   } else if (warp >= 6) {
-    // ======================= softmax, conversions, stores =======================
+    // ======================= softmax, normalisation, q' conversion =======================
     const int qd = warp & 3;
     const int half = (warp - 6) >> 2;
     const int r_ = qd * 32 + lane;
@@ -1850,13 +1948,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t red_other = red_mine ^ (128u * 4u);      // the partner warp's slot
     const uint32_t bar_id = 1u + (uint32_t)qd;
     const int oc0 = half * (RC / 2);
-    const int nq = dh / 2;                                   // output columns of this warp
-    if (warp == 6 && lane == 0) {
-      // receive barriers of the first four tiles and of item 0's partial output
+    if (warp == 6 && lane == 0)            // receive barriers of the first four tiles
       for (int xb = 0; xb < kXBuf; ++xb)
         mbar_arrive_expect_tx(&bars->x_full[xb], (uint32_t)kXBytes);
-      mbar_arrive_expect_tx(&bars->epi_x, epi_x_bytes(dh));
-    }
     __syncwarp();
     if (lane == 0) {                       // initial release of buffers 2 and 3 (0 and 1
       mbar_arrive(&bars->x_consumed[2]);   // hold item 0's q tile)
@@ -1865,91 +1959,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int T = 0;
     bool ok = true;
     PItem it;
-    for (int r = 0; ok; ++r) {
-      const bool have = pair_item(a, r, it);
-      // ---- boundary: item r's q' into TMEM, item r-1's output out ----
-      if (have) {
-        if (!(ok = warp_wait(&bars->pro_done, r & 1, 99, abort_flag))) break;
-        tc_fence_after();
-        tmem_rows_to_bf16(tmem + lane_base + kTmemO + oc0, tmem + lane_base + kTmemQ + oc0 / 2,
-                          RC / 2, a.qscale);
+    for (int r = 0; ok && pair_item(a, r, it); ++r) {
+      // ---- item r's q' (fp32 in O's columns, scaled by scale*log2 e) -> bf16 in TMEM ----
+      if (!(ok = warp_wait(&bars->pro_done, r & 1, 99, abort_flag))) break;
+      tc_fence_after();
+      tmem_rows_to_bf16(tmem + lane_base + kTmemO + oc0, tmem + lane_base + kTmemQ + oc0 / 2,
+                        RC / 2, a.qscale);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->q_ready);
+      __syncwarp();
+      if (lane == 0) {                       // the absorption has read the q buffers
+        mbar_arrive(&bars->x_consumed[T & 3]);
+        mbar_arrive(&bars->x_consumed[(T + 1) & 3]);
       }
-      float ov[2][16];
-      // first output column of this warp (re-read here, not kept across the tiles)
-      const int cfirst = (int)cluster_ctarank() * dh + half * nq;
-      if (r > 0) {
-        if (!(ok = warp_wait(&bars->epi_done, (r - 1) & 1, 100, abort_flag))) break;
-        tc_fence_after();
-        tmem_ld16(tmem + lane_base + kTmemS + cfirst, ov[0]);
-        if (nq > 16) tmem_ld16(tmem + lane_base + kTmemS + cfirst + 16, ov[1]);
-        tmem_wait_ld();
-      }
-      if (have) {
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->q_ready);
-        __syncwarp();
-        if (lane == 0) {                     // the absorption has read the q buffers
-          mbar_arrive(&bars->x_consumed[T & 3]);
-          mbar_arrive(&bars->x_consumed[(T + 1) & 3]);
-        }
-      }
-      if (r > 0) {
-        // the peer's partial product for my columns, fp16 rows times 2^k
-        if (!(ok = warp_wait<true>(&bars->epi_x, (r - 1) & 1, 101, abort_flag))) break;
-        const uint32_t xo = x_local + (uint32_t)((T + 2) & 3) * kXBytes;
-        const uint32_t xs = x_local + (uint32_t)((T + 3) & 3) * kXBytes;
-        float inv_sc, y0, y1, y2;
-        ld_shared_v4f(xs + (uint32_t)r_ * 16, inv_sc, y0, y1, y2);
-        const int cc0 = half * nq;            // first column within the received half
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {         // 8 fp16 per 16-byte chunk
-          if (q * 8 < nq) {
-            float x[4];
-            ld_shared_v4f(xo + xrow_offset((uint32_t)r_, (uint32_t)((cc0 >> 3) + q), 128u), x[0],
-                          x[1], x[2], x[3]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = unpack_half2(__float_as_uint(x[e]));
-              ov[q >> 1][8 * (q & 1) + 2 * e] += f.x * inv_sc;
-              ov[q >> 1][8 * (q & 1) + 2 * e + 1] += f.y * inv_sc;
-            }
-          }
-        }
-        if (have && warp == 6 && lane == 0)  // item r's partial output comes next
-          mbar_arrive_expect_tx(&bars->epi_x, epi_x_bytes(dh));
-        __syncwarp();
-        if (have && lane == 0) {             // the partial-output buffers are free
-          mbar_arrive(&bars->x_consumed[(T + 2) & 3]);
-          mbar_arrive(&bars->x_consumed[(T + 3) & 3]);
-        }
-        PItem prev;
-        pair_item(a, r - 1, prev);
-        const int pgrow = prev.row0 + r_;
-        if (pgrow < a.Tq) {
-          const int64_t orow = (((int64_t)prev.b * a.Tq + pgrow) * a.H + prev.head) * a.d + cfirst;
-          if (a.out_bf16) {
-            uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (q * 8 < nq) {
-                const float* w = &ov[q >> 1][8 * (q & 1)];
-                d4[q] = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
-                                   pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
-              }
-          } else {
-            float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (q * 4 < nq) {
-                const float* w = &ov[q >> 2][4 * (q & 3)];
-                d4[q] = make_float4(w[0], w[1], w[2], w[3]);
-              }
-          }
-        }
-      }
-      if (!have) break;
-
       // ---- the item's tiles ----
       // keys visible to my row: key < lim (none for a row past the end)
       const int grow = it.row0 + r_;
@@ -2035,6 +2058,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
+        // the previous item's output staging has been read out of the P buffers
+        if (g == T && r > 0 &&
+            !(ok = warp_wait(&bars->stg_free, (r - 1) & 1, 107, abort_flag)))
+          break;
         const uint32_t pb = smem_u32(smem + kOffP + bi * kPBytes);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -2242,7 +2269,6 @@ cudaError_t launch_flash_persistent(const CUtensorMap& mapQ, const CUtensorMap& 
   }
 }
 
-template <int kRC>
 static cudaLaunchConfig_t pair_config(int pairs, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
@@ -2262,16 +2288,16 @@ static cudaLaunchConfig_t pair_config(int pairs, cudaStream_t stream, cudaLaunch
 
 // CTA pairs of the persistent pair kernel that fit on the current device at
 // once (a cluster needs two free SMs of one GPC), 0 if the query fails.
-template <int kRC>
+template <int kRC, int kD>
 static int pair_slots_rc() {
-  auto kern = flash_persistent_pair_kernel<kRC>;
+  auto kern = flash_persistent_pair_kernel<kRC, kD>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = pair_config<kRC>(1, nullptr, attr);
+  const cudaLaunchConfig_t cfg = pair_config(1, nullptr, attr);
   int clusters = 0;
   if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();
@@ -2280,50 +2306,58 @@ static int pair_slots_rc() {
   return clusters;
 }
 
-int flash_pair_slots(int RC) {
+int flash_pair_slots(int RC, int d) {
   constexpr int kDevices = 64;
-  static std::atomic<int> cache[2][kDevices];   // 0: not yet queried, else slots + 1
-  if (RC != 192 && RC != 256) return 0;
+  static std::atomic<int> cache[4][kDevices];   // 0: not yet queried, else slots + 1
+  if ((RC != 192 && RC != 256) || (d != 64 && d != 128)) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) {
     cudaGetLastError();
     return 0;
   }
-  std::atomic<int>& c = cache[RC == 256 ? 1 : 0][dev];
+  const int k = (RC == 256 ? 2 : 0) + (d == 128 ? 1 : 0);
+  std::atomic<int>& c = cache[k][dev];
   int v = c.load(std::memory_order_relaxed);
   if (v == 0) {
-    v = (RC == 256 ? pair_slots_rc<256>() : pair_slots_rc<192>()) + 1;
-    c.store(v, std::memory_order_relaxed);
+    switch (k) {
+      case 0: v = pair_slots_rc<192, 64>(); break;
+      case 1: v = pair_slots_rc<192, 128>(); break;
+      case 2: v = pair_slots_rc<256, 64>(); break;
+      default: v = pair_slots_rc<256, 128>(); break;
+    }
+    c.store(v + 1, std::memory_order_relaxed);
+    return v;
   }
   return v - 1;
 }
 
-template <int kRC>
+template <int kRC, int kD>
 static cudaError_t launch_persistent_pair_rc(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                              const CUtensorMap& mapWk, const CUtensorMap& mapWv,
-                                             const FlashArgs& args, int pairs,
-                                             cudaStream_t stream) {
-  auto kern = flash_persistent_pair_kernel<kRC>;
+                                             const CUtensorMap& mapO, const FlashArgs& args,
+                                             int pairs, cudaStream_t stream) {
+  auto kern = flash_persistent_pair_kernel<kRC, kD>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = pair_config<kRC>(pairs, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, args);
+  const cudaLaunchConfig_t cfg = pair_config(pairs, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, mapO, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_flash_persistent_pair(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                          const CUtensorMap& mapWk, const CUtensorMap& mapWv,
-                                         const FlashArgs& args, int pairs, cudaStream_t stream) {
-  if (!args.pair || (args.d != 64 && args.d != 128) || args.cu_q != nullptr || pairs <= 0)
-    return cudaErrorInvalidValue;
-  switch (args.RC) {
-    case 192:
-      return launch_persistent_pair_rc<192>(mapQ, mapL, mapWk, mapWv, args, pairs, stream);
-    case 256:
-      return launch_persistent_pair_rc<256>(mapQ, mapL, mapWk, mapWv, args, pairs, stream);
+                                         const CUtensorMap& mapO, const FlashArgs& args,
+                                         int pairs, cudaStream_t stream) {
+  if (!args.pair || args.cu_q != nullptr || pairs <= 0) return cudaErrorInvalidValue;
+  const int k = (args.RC == 256 ? 2 : args.RC == 192 ? 0 : -8) + (args.d == 128 ? 1 : args.d == 64 ? 0 : -8);
+  switch (k) {
+    case 0: return launch_persistent_pair_rc<192, 64>(mapQ, mapL, mapWk, mapWv, mapO, args, pairs, stream);
+    case 1: return launch_persistent_pair_rc<192, 128>(mapQ, mapL, mapWk, mapWv, mapO, args, pairs, stream);
+    case 2: return launch_persistent_pair_rc<256, 64>(mapQ, mapL, mapWk, mapWv, mapO, args, pairs, stream);
+    case 3: return launch_persistent_pair_rc<256, 128>(mapQ, mapL, mapWk, mapWv, mapO, args, pairs, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -94,14 +94,18 @@ cudaError_t launch_flash_persistent(const CUtensorMap& mapQ, const CUtensorMap& 
                                     const FlashArgs& args, int num_ctas, cudaStream_t stream);
 
 // Persistent CTA-pair prefill (rank 384 or 512, d = 64 or 128, dense batch):
-// `pairs` resident clusters of two CTAs (at most flash_pair_slots(RC)) work
-// through the items; maps as launch_flash_persistent; results bitwise equal to
-// launch_flash_fused's.  flash_pair_slots returns how many such pairs fit on
-// the current device at once (cached per device), 0 when unknown.
-int flash_pair_slots(int RC);
+// `pairs` resident clusters of two CTAs (at most flash_pair_slots(RC, d)) work
+// through the items; maps as launch_flash_fused except the output map, which is
+// 4-D ({d, H, Tq, B}, 128-byte swizzle, box {128 / element bytes, 1, 128, 1}) so
+// that the tile stores of a partial row block stop at its sequence's end;
+// results bitwise equal to launch_flash_fused's.  flash_pair_slots returns how
+// many such pairs fit on the current device at once (cached per device), 0
+// when unknown.
+int flash_pair_slots(int RC, int d);
 cudaError_t launch_flash_persistent_pair(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                          const CUtensorMap& mapWk, const CUtensorMap& mapWv,
-                                         const FlashArgs& args, int pairs, cudaStream_t stream);
+                                         const CUtensorMap& mapO, const FlashArgs& args,
+                                         int pairs, cudaStream_t stream);
 
 cudaError_t launch_merge_partials(const float* m_l, int ml_stride, const float* l, const float* o,
                                   void* out, int parts, int rows, int width, int out_bf16,

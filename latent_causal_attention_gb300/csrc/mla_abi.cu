@@ -62,6 +62,24 @@ static bool make_out_tmap(CUtensorMap* map, void* out, bool bf16, int d, int H, 
                       (uint64_t)H * d * es, 128u / es, 1, 128, true);
 }
 
+// The persistent pair kernel's output tiles: out (B, Tq, H, d) as {d, H, Tq, B},
+// so that a tile store never crosses into the next batch entry.
+static bool make_out_tmap_4d(CUtensorMap* map, void* out, bool bf16, int d, int H, int Tq,
+                             int B) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t es = bf16 ? 2 : 4;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)Tq, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {d * es, (uint64_t)H * d * es, (uint64_t)Tq * H * d * es};
+  const cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  4, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------
 // Options
 // ---------------------------------------------------------------------------
@@ -408,12 +426,13 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
     }
     if (g_persistent && p.pair) {
       // one resident CTA pair per two SMs (as many as fit at once)
-      int64_t pairs = flash_pair_slots(p.RC);
+      int64_t pairs = flash_pair_slots(p.RC, d);
       if (pairs > planner_sm_count() / 2) pairs = planner_sm_count() / 2;
       if (pairs > items) pairs = items;
-      if (pairs > 0) {
+      CUtensorMap mO4;
+      if (pairs > 0 && make_out_tmap_4d(&mO4, out, out_dtype == MLA_BF16, d, H, Tq, B)) {
         if (staged(1, stream, [&] {
-              return launch_flash_persistent_pair(mQ, mL, mWk, mWv, fa, (int)pairs, stream);
+              return launch_flash_persistent_pair(mQ, mL, mWk, mWv, mO4, fa, (int)pairs, stream);
             }) != cudaSuccess)
           return MLA_ERR_CUDA;
         return MLA_OK;
