@@ -1452,7 +1452,7 @@ struct QBars {
   uint64_t pro_done;           // absorption MMA done
   uint64_t q_ready;            // q' in TMEM, O zeroed, the previous output read (softmax + exchange)
   uint64_t o_last;             // the item's S and O MMAs have completed (two issuers)
-  uint64_t epi_a;              // normalised O_lat (bf16) in q''s columns
+  uint64_t epi_a;              // normalised O_lat (bf16) in q''s columns, the item's last S read
   uint64_t epi_done;           // output MMA done
   uint64_t x_full[kXBuf];      // my receive buffer b holds the peer's partial S of a tile
   uint64_t x_empty[kXBuf];     // the peer's receive buffer b may be used again
@@ -1471,8 +1471,8 @@ static_assert(offsetof(QBars, s_empty) == 10 * 8 && offsetof(QBars, p_full) == 1
 static_assert(sizeof(QBars) <= kBarBytes, "pair persistent barrier block");
 
 __device__ __forceinline__ uint32_t qbar_arrivals(int i) {
-  if (i == 10 || i == 11 || i == 18) return 384;     // s_empty, q_ready
-  if (i == 12 || i == 13 || i == 20) return 256;     // p_full, epi_a
+  if (i == 10 || i == 11 || i == 18 || i == 20) return 384;   // s_empty, q_ready, epi_a
+  if (i == 12 || i == 13) return 256;                         // p_full
   if (i == 19) return 2;                             // o_last
   if (i >= 30 && i <= 33) return 8;                  // x_consumed
   return 1;
@@ -1556,14 +1556,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       PItem it;
       for (int r = 0; ok && pair_item(a, r, it); ++r) {
-        // w_up_k rows of this CTA's rank columns, one slot per 64 d columns
+        // w_up_k rows of this CTA's rank columns, one slot per 64 d columns; every
+        // chunk completes on the first slot's barrier (the others just arrive)
         for (int kc = 0; ok && kc < dch; ++kc) {
-          const int slot = S + kc, st = slot % kStages;
-          if (!(ok = mbar_wait(&bars->l_empty[st], ((slot / kStages) & 1) ^ 1, 80, abort_flag)))
-            break;
-          mbar_arrive_expect_tx(&bars->l_full[st], (uint32_t)(RC * 128));
-          tma_load_3d(sL + st * kLStage, &mapWk, &bars->l_full[st], 64 * kc, it.head, c0);
-          hi = slot + 1;
+          const int slot = S + kc;
+          ok = mbar_wait(&bars->l_empty[slot % kStages], ((slot / kStages) & 1) ^ 1, 80,
+                         abort_flag);
+        }
+        if (!ok) break;
+        {
+          uint64_t* bar = &bars->l_full[S % kStages];
+          mbar_arrive_expect_tx(bar, (uint32_t)(dch * RC * 128));
+          for (int kc = 1; kc < dch; ++kc) mbar_arrive(&bars->l_full[(S + kc) % kStages]);
+          for (int kc = 0; kc < dch; ++kc)
+            tma_load_3d(sL + ((S + kc) % kStages) * kLStage, &mapWk, bar, 64 * kc, it.head, c0);
+          hi = S + dch;
         }
         S += dch;
         for (int j = 0; ok && j < it.nt; ++j) {
@@ -1585,12 +1592,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         const EpiStages ws = wv_stages(S, dch);
-        for (int nc = 0; nc < dch; ++nc) {
-          uint64_t* bar = &bars->l_full[(S + nc) % kStages];
-          mbar_arrive_expect_tx(bar, (uint32_t)(RC * 128));
-          for (int kb = 0; kb < RC / 64; ++kb)
-            tma_load_3d(sL + ws.wv_lo * kLStage + nc * ws.wv_lbo + kb * (64 * 128), &mapWv, bar,
-                        64 * nc, it.head, c0 + 64 * kb);
+        {
+          uint64_t* bar = &bars->l_full[S % kStages];     // all chunks on the first slot's
+          mbar_arrive_expect_tx(bar, (uint32_t)(dch * RC * 128));
+          for (int nc = 1; nc < dch; ++nc) mbar_arrive(&bars->l_full[(S + nc) % kStages]);
+          for (int nc = 0; nc < dch; ++nc)
+            for (int kb = 0; kb < RC / 64; ++kb)
+              tma_load_3d(sL + ws.wv_lo * kLStage + nc * ws.wv_lbo + kb * (64 * 128), &mapWv, bar,
+                          64 * nc, it.head, c0 + 64 * kb);
         }
         hi = S + dch;
         S += dch;
@@ -1612,16 +1621,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t l0 = smem_u32(sL), p0 = smem_u32(smem + kOffP), x0 = smem_u32(sX);
       const uint32_t tq = tmem + kTmemQ;
       // output MMA of an item: out_partial = O_lat(bf16, q''s columns) . w_up_v into
-      // S's columns, once the normalisation is done and the item's last two S tiles
-      // have been read
-      auto output_mma = [&](int r, int wv_slot, int t_end) -> bool {
-        bool good = mbar_wait(&bars->epi_a, r & 1, 84, abort_flag);
-        for (int g = max(t_end - 2, 0); good && g < t_end; ++g)
-          good = mbar_wait(&bars->s_empty[g & 1], (g >> 1) & 1, 85, abort_flag);
-        for (int nc = 0; good && nc < dch; ++nc) {
-          const int slot = wv_slot + nc;
-          good = mbar_wait(&bars->l_full[slot % kStages], (slot / kStages) & 1, 86, abort_flag);
-        }
+      // S's columns, once the normalisation is done and the item's last S tiles have
+      // been read (epi_a) and w_up_v has landed (the first slot's barrier)
+      auto output_mma = [&](int r, int wv_slot) -> bool {
+        const bool good =
+            mbar_wait(&bars->epi_a, r & 1, 84, abort_flag) &&
+            mbar_wait(&bars->l_full[wv_slot % kStages], (wv_slot / kStages) & 1, 86, abort_flag);
         if (!good) {
           umma_commit(&bars->epi_done);
           return false;
@@ -1643,14 +1648,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; ok && pair_item(a, r, it); ++r) {
         const int wk_slot = S, l_slot = S + dch;
         if (warp == 1) {
-          if (r > 0) ok = output_mma(r - 1, prev_wv, T);
+          if (r > 0) ok = output_mma(r - 1, prev_wv);
           // q' (fp32, this CTA's rank columns) = q . w_up_k^T into O's columns; A = the
           // q tile in receive buffers T%4 and (T+1)%4, B = the w_up_k slots
-          ok = ok && mbar_wait(&bars->pro_full, r & 1, 87, abort_flag);
-          for (int kc = 0; ok && kc < dch; ++kc) {
-            const int slot = wk_slot + kc;
-            ok = mbar_wait(&bars->l_full[slot % kStages], (slot / kStages) & 1, 88, abort_flag);
-          }
+          ok = ok && mbar_wait(&bars->pro_full, r & 1, 87, abort_flag) &&
+               mbar_wait(&bars->l_full[wk_slot % kStages], (wk_slot / kStages) & 1, 88, abort_flag);
           if (ok) {
             tc_fence_after();
             for (int kc = 0; kc < dch; ++kc) {
@@ -1707,7 +1709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         T += it.nt;
         S = l_slot + it.nt + dch;
       }
-      if (warp == 1 && ok && r > 0) output_mma(r - 1, prev_wv, T);
+      if (warp == 1 && ok && r > 0) output_mma(r - 1, prev_wv);
     }
   } else if (warp < 6) {
     // ======================= exchange with the peer =======================
@@ -1892,6 +1894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pack_half2(s2[hh][8 * c + 4], s2[hh][8 * c + 5]),
                          pack_half2(s2[hh][8 * c + 6], s2[hh][8 * c + 7]), bar);
       }
+      if (ok) mbar_arrive(&bars->epi_a);     // the item's S columns may be overwritten
       T += it.nt;
     }
   } else if (warp == 14) {
