@@ -794,7 +794,7 @@ def time_small(dev, n: int = 200, warmup: int = 20):
 
 
 def run_attention_only(args, name: str):
-    """Only one workload's attention (decode_bf16 or mid_bf16): warm-up, then
+    """Only one workload's attention (decode_bf16, mid_bf16 or prefill_bf16): warm-up, then
     timed calls with the L2 flushed between them; one JSON line.  A small
     driver for profiling that workload's kernels."""
     import torch
@@ -836,11 +836,14 @@ def main():
                     help="time only the decode attention (a driver for profiling its kernels)")
     ap.add_argument("--mid-only", action="store_true",
                     help="time only the mid-size attention (a driver for profiling its kernel)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prefill attention (a driver for profiling its kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.decode_only or args.mid_only:
-        run_attention_only(args, "decode_bf16" if args.decode_only else "mid_bf16")
+    if args.decode_only or args.mid_only or args.prefill_only:
+        run_attention_only(args, "decode_bf16" if args.decode_only else
+                           "mid_bf16" if args.mid_only else "prefill_bf16")
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -1014,10 +1014,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ring, w_up_v into the ring slot after the item's last tile); warp 1 lane 0
 // the absorption MMA, the S MMAs of even tiles and the output MMA; warp 15
 // lane 0 the S MMAs of odd tiles; warp 2 lane 0 the O MMAs; warps 6-13
-// softmax and epilogue.  Item boundary: the softmax warps normalise O_lat
-// into q''s columns (epi_a), warp 1 issues the output MMA and then the next
-// item's absorption into O's columns, the softmax warps read the output from
-// S's columns, store it, turn the next q' into bf16 and zero O (q_ready).
+// softmax, normalisation and q' conversion; warps 3, 4, 5 and 14 (one per
+// TMEM lane quadrant) the output.  Item boundary: the softmax warps normalise
+// O_lat into q''s columns (epi_a), warp 1 issues the output MMA and then the
+// next item's absorption into O's columns; the output warps read the output
+// from S's columns, stage it in the P buffers and write it with tile stores
+// (stg_free once read out); the softmax warps turn the next q' into bf16 and
+// zero O (q_ready, with the output warps' read) and write their next P only
+// after stg_free.
 //
 // Items are dealt in rounds of gridDim.x, heavy row blocks first, alternating
 // direction every round (CTA c takes items c, 2G-1-c, 2G+c, ...), which
@@ -1040,18 +1044,21 @@ struct PBars {
   uint64_t epi_done;           // output MMA done
   uint64_t epi_w[2];           // w_up_v of item r staged (TMA), by item parity: the
                                // producer may stage item r+1's before item r's is used
+  uint64_t stg_free;           // the item's output staging (P buffers) has been read out
   uint32_t tmem_slot;
   int abort_flag;
 };
-constexpr int kPNumBars = 24;
+constexpr int kPNumBars = 25;
 static_assert(offsetof(PBars, s_empty) == 10 * 8 && offsetof(PBars, p_full) == 12 * 8 &&
                   offsetof(PBars, q_ready) == 18 * 8 && offsetof(PBars, o_last) == 19 * 8 &&
-                  offsetof(PBars, epi_a) == 20 * 8 && offsetof(PBars, epi_w) == 22 * 8,
+                  offsetof(PBars, epi_a) == 20 * 8 && offsetof(PBars, epi_w) == 22 * 8 &&
+                  offsetof(PBars, stg_free) == 24 * 8,
               "persistent barrier indices");
 static_assert(sizeof(PBars) <= kBarBytes, "persistent barrier block");
 
 __device__ __forceinline__ uint32_t pbar_arrivals(int i) {
-  if (i == 10 || i == 11 || i == 12 || i == 13 || i == 18 || i == 20) return 256;
+  if (i == 18) return 384;                         // q_ready: softmax + output warps
+  if (i == 10 || i == 11 || i == 12 || i == 13 || i == 20) return 256;
   if (i == 19) return 3;
   return 1;
 }
@@ -1082,7 +1089,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     flash_persistent_kernel(const __grid_constant__ CUtensorMap mapQ,
                             const __grid_constant__ CUtensorMap mapL,
                             const __grid_constant__ CUtensorMap mapWk,
-                            const __grid_constant__ CUtensorMap mapWv, FlashArgs a) {
+                            const __grid_constant__ CUtensorMap mapWv,
+                            const __grid_constant__ CUtensorMap mapO, FlashArgs a) {
   extern __shared__ uint8_t flash_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(flash_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1341,6 +1349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
+        // the previous item's output staging has been read out of the P buffers
+        if (j == 0 && r > 0 && !(ok = warp_wait(&bars->stg_free, (r - 1) & 1, 78, abort_flag)))
+          break;
         const uint32_t pb = smem_u32(sP + bi * kPBytes);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -1367,28 +1378,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->epi_a);
-      if (!(ok = warp_wait(&bars->epi_done, r & 1, 76, abort_flag))) break;
-      tc_fence_after();
-      // out[b, i, h, half*32 .. +32]: my row's half of the head's 64 values
-      float v[32];
-      tmem_ld32(tmem + lane_base + kTmemS + half * 32, v);
-      tmem_wait_ld();
-      if (row_valid) {
-        const int64_t orow = (((int64_t)it.b * a.Tq + grow) * a.H + it.head) * 64 + half * 32;
-        if (a.out_bf16) {
-          uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                               pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-        } else {
-          float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
-      }
       T += it.nt;
+    }
+  } else if ((warp >= 3 && warp <= 5) || warp == 14) {
+    // ======================= item outputs =======================
+    // out[b, i, h, 0..64) of the previous item by tile stores of 128 x 128-byte
+    // boxes staged (128-byte swizzle) in the P buffers, free between the item's
+    // last O MMA and the next item's first P; the map is per batch entry, so the
+    // rows of a partial block past the sequence's end are not written
+    const int qd = warp & 3;                       // lane quadrant of this warp
+    const uint32_t rr = (uint32_t)(qd * 32 + lane);
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const uint32_t row = smem_u32(sP) + rr * 128, sw = rr & 7;
+    bool ok = true;
+    PItem it;
+    for (int r = 0; ok; ++r) {
+      const bool have = persist_item(a, r, (int)gridDim.x, (int)blockIdx.x, it);
+      if (r > 0) {
+        if (!(ok = warp_wait(&bars->epi_done, (r - 1) & 1, 76, abort_flag))) break;
+        tc_fence_after();
+        float v[2][32];
+        tmem_ld32(tmem + lane_base + kTmemS, v[0]);
+        tmem_ld32(tmem + lane_base + kTmemS + 32, v[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        if (have) mbar_arrive(&bars->q_ready);   // item r's S may overwrite the output
+        PItem prev;
+        persist_item(a, r - 1, (int)gridDim.x, (int)blockIdx.x, prev);
+        if (a.out_bf16) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float* w = &v[q >> 2][8 * (q & 3)];
+            st_shared_v4(row + ((((uint32_t)q) ^ sw) << 4), pack_bf16x2(w[0], w[1]),
+                         pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                         pack_bf16x2(w[6], w[7]));
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float* w = &v[q >> 3][4 * (q & 7)];
+            st_shared_v4(row + (uint32_t)(q >> 3) * (kRows * 128) + ((((uint32_t)q & 7u) ^ sw) << 4),
+                         __float_as_uint(w[0]), __float_as_uint(w[1]), __float_as_uint(w[2]),
+                         __float_as_uint(w[3]));
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(6, 128);                    // all four warps have staged their rows
+        if (warp == 3 && lane == 0) {
+          const int nbox = a.out_bf16 ? 1 : 2;
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_store_4d(&mapO, smem_u32(sP) + (uint32_t)bx * (kRows * 128), bx * (64 / nbox),
+                         prev.head, prev.row0, prev.b);
+          bulk_commit_group();
+          bulk_wait_read_all();                    // the staging must outlive the reads
+          mbar_arrive(&bars->stg_free);
+        }
+      } else if (have) {
+        mbar_arrive(&bars->q_ready);
+      }
+      if (!have) break;
     }
   }
 
@@ -2237,8 +2285,8 @@ cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
 template <int kRC>
 static cudaError_t launch_persistent_rc(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                         const CUtensorMap& mapWk, const CUtensorMap& mapWv,
-                                        const FlashArgs& args, int num_ctas,
-                                        cudaStream_t stream) {
+                                        const CUtensorMap& mapO, const FlashArgs& args,
+                                        int num_ctas, cudaStream_t stream) {
   auto kern = flash_persistent_kernel<kRC>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -2253,21 +2301,22 @@ static cudaError_t launch_persistent_rc(const CUtensorMap& mapQ, const CUtensorM
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, args);
+  e = cudaLaunchKernelEx(&cfg, kern, mapQ, mapL, mapWk, mapWv, mapO, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_flash_persistent(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                     const CUtensorMap& mapWk, const CUtensorMap& mapWv,
-                                    const FlashArgs& args, int num_ctas, cudaStream_t stream) {
+                                    const CUtensorMap& mapO, const FlashArgs& args, int num_ctas,
+                                    cudaStream_t stream) {
   if (args.pair || args.d != 64 || args.cu_q != nullptr || num_ctas <= 0)
     return cudaErrorInvalidValue;
   switch (args.RC) {
-    case 64: return launch_persistent_rc<64>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
-    case 128: return launch_persistent_rc<128>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
-    case 192: return launch_persistent_rc<192>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
-    case 256: return launch_persistent_rc<256>(mapQ, mapL, mapWk, mapWv, args, num_ctas, stream);
+    case 64: return launch_persistent_rc<64>(mapQ, mapL, mapWk, mapWv, mapO, args, num_ctas, stream);
+    case 128: return launch_persistent_rc<128>(mapQ, mapL, mapWk, mapWv, mapO, args, num_ctas, stream);
+    case 192: return launch_persistent_rc<192>(mapQ, mapL, mapWk, mapWv, mapO, args, num_ctas, stream);
+    case 256: return launch_persistent_rc<256>(mapQ, mapL, mapWk, mapWv, mapO, args, num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -87,11 +87,14 @@ cudaError_t launch_flash_fused(const CUtensorMap& mapQ, const CUtensorMap& mapL,
 
 // Persistent single-CTA prefill (rank <= 256, d = 64, dense batch): num_ctas
 // resident CTAs work through the (batch entry, head, 128-row block) items; same
-// tensor maps as the fused prefill minus the output map (rows are stored
-// directly); results bitwise equal to launch_flash_fused's.
+// tensor maps as the fused prefill except the output map, which is 4-D
+// ({d, H, Tq, B}, 128-byte swizzle, box {128 / element bytes, 1, 128, 1}) so
+// that the tile stores of a partial row block stop at its sequence's end;
+// results bitwise equal to launch_flash_fused's.
 cudaError_t launch_flash_persistent(const CUtensorMap& mapQ, const CUtensorMap& mapL,
                                     const CUtensorMap& mapWk, const CUtensorMap& mapWv,
-                                    const FlashArgs& args, int num_ctas, cudaStream_t stream);
+                                    const CUtensorMap& mapO, const FlashArgs& args, int num_ctas,
+                                    cudaStream_t stream);
 
 // Persistent CTA-pair prefill (rank 384 or 512, d = 64 or 128, dense batch):
 // `pairs` resident clusters of two CTAs (at most flash_pair_slots(RC, d)) work

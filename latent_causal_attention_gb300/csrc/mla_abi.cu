@@ -415,11 +415,13 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
     fa.d = d; fa.qscale = scale * 1.4426950408889634f; fa.out = out;
     fa.out_bf16 = out_dtype == MLA_BF16;
     const int64_t items = (int64_t)p.row_blocks * B * H;
-    if (g_persistent && !p.pair && d == 64) {
+    CUtensorMap mO4;
+    const bool have_o4 = make_out_tmap_4d(&mO4, out, out_dtype == MLA_BF16, d, H, Tq, B);
+    if (g_persistent && !p.pair && d == 64 && have_o4) {
       // one resident CTA per SM works through the (b, head, row block) items
       const int ctas = (int)(items < planner_sm_count() ? items : planner_sm_count());
       if (staged(1, stream, [&] {
-            return launch_flash_persistent(mQ, mL, mWk, mWv, fa, ctas, stream);
+            return launch_flash_persistent(mQ, mL, mWk, mWv, mO4, fa, ctas, stream);
           }) != cudaSuccess)
         return MLA_ERR_CUDA;
       return MLA_OK;
@@ -429,8 +431,7 @@ mla_status_t mla_latent_attention(const void* q, const void* kv_latent, const vo
       int64_t pairs = flash_pair_slots(p.RC, d);
       if (pairs > planner_sm_count() / 2) pairs = planner_sm_count() / 2;
       if (pairs > items) pairs = items;
-      CUtensorMap mO4;
-      if (pairs > 0 && make_out_tmap_4d(&mO4, out, out_dtype == MLA_BF16, d, H, Tq, B)) {
+      if (pairs > 0 && have_o4) {
         if (staged(1, stream, [&] {
               return launch_flash_persistent_pair(mQ, mL, mWk, mWv, mO4, fa, (int)pairs, stream);
             }) != cudaSuccess)

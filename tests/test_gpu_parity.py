@@ -537,15 +537,15 @@ PERSIST = [
     dict(B=2, Tq=300, Tkv=300, H=4, d=64, rank=256, causal=True),     # ragged row blocks
     dict(B=1, Tq=200, Tkv=700, H=3, d=64, rank=128, causal=True),     # chunked prefill
     dict(B=3, Tq=128, Tkv=128, H=2, d=64, rank=64, causal=False),     # no mask
-    dict(B=1, Tq=1024, Tkv=1024, H=40, d=64, rank=192, causal=True),  # 320 items: several rounds
+    dict(B=4, Tq=256, Tkv=256, H=40, d=64, rank=192, causal=True),    # 320 items: three rounds
     # CTA pairs (rank > 256): items of one to five tiles, so that every receive
     # buffer takes q tiles and partial outputs in turn
     dict(B=2, Tq=300, Tkv=300, H=3, d=128, rank=512, causal=True),    # ragged, 2..5 tiles
     dict(B=1, Tq=200, Tkv=700, H=2, d=64, rank=384, causal=True),     # chunked, d 64, RC 192
     dict(B=3, Tq=64, Tkv=64, H=2, d=128, rank=512, causal=True),      # one-tile items
     dict(B=2, Tq=130, Tkv=130, H=2, d=128, rank=512, causal=False),   # no mask, 3-tile items
-    dict(B=1, Tq=1024, Tkv=1024, H=40, d=128, rank=512, causal=True), # 320 items: several rounds
-    dict(B=1, Tq=640, Tkv=640, H=36, d=64, rank=384, causal=True),    # 180 items, RC 192
+    dict(B=4, Tq=256, Tkv=256, H=40, d=128, rank=512, causal=True),   # 320 items: five rounds
+    dict(B=2, Tq=320, Tkv=320, H=30, d=64, rank=384, causal=True),    # 180 items, RC 192
 ]
 
 
