@@ -652,7 +652,8 @@ def run_ours(args, rank: int, world: int):
                                  * args.steps * world / (total_ms * 1e-3) / 1e12, 3)},
         "frac_of_peak_step": round(value / world / peak, 4),
         "roofline": {"bound": "tensor",
-                     "kernel": "flash_packed_kernel<256, fused>" if fused else "flash_packed_kernel",
+                     "kernel": ("flash_persistent_pair_kernel<256, 128> (resident CTA pairs, "
+                                "the whole fused attention)") if fused else "flash_packed_kernel",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} bf16 dense (burst)",
