@@ -146,8 +146,9 @@ int mla_latent_attention_kv_splits(int B, int Tq, int Tkv, int H, int d, int ran
  *     latent space, flash loop over TMA-staged latent tiles with tcgen05).
  *     With Tq >= 64 and d <= 128 it is one fused kernel per (head, 128
  *     query positions) that also does the absorption and w_up_v and needs no
- *     workspace (for rank <= 256 and d == 64 one resident CTA per SM works
- *     through those row blocks); otherwise absorption GEMM, head-packed flash
+ *     workspace (on a dense batch, for rank <= 256 and d == 64 one resident
+ *     CTA per SM, for rank 384 or 512 one resident CTA pair per two SMs,
+ *     works through those row blocks); otherwise absorption GEMM, head-packed flash
  *     loop (split over the key range when there are few rows), merge and
  *     w_up_v GEMM.
  *   - otherwise (fp32, or small/odd shapes): warp-per-query CUDA-core path
@@ -292,9 +293,11 @@ typedef enum {
                                   0 always the head-packed kernels                    */
   MLA_OPT_NUM_SMS = 3,         /* 0 (default) plan for the device's own SM count,
                                   n > 0 plan for n SMs                                */
-  MLA_OPT_PERSISTENT = 4       /* 1 (default) long prefill with rank <= 256 and d == 64
-                                  runs one resident CTA per SM over all row blocks;
-                                  0 one CTA per row block (same results bit for bit)  */
+  MLA_OPT_PERSISTENT = 4       /* 1 (default) long prefill of a dense batch runs
+                                  resident CTAs (rank <= 256, d == 64) or resident
+                                  CTA pairs (rank 384 / 512, d 64 / 128) over all row
+                                  blocks; 0 one CTA (pair) per row block (same
+                                  results bit for bit)                               */
 } mla_option_t;
 mla_status_t mla_set_option(int option, int64_t value);
 
