@@ -718,11 +718,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             s[8 * c + 2 * e + 1] = t.y;
           }
         }
-        // re-arm this buffer's barrier for tile j+kXBuf (its phase for tile j is complete)
-        if (warp == 6 && lane == 0 && j + kXBuf < nt)
-          mbar_arrive_expect_tx(&bars->x_full[xb], (uint32_t)kXBytes);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->x_consumed[xb]);
       }
 
       // mask: key s_idx visible iff s_idx < Tkv and (not causal or s_idx <= t)
@@ -789,6 +784,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_full[bi]);
+      if (a.pair) {
+        // the receive buffer is released off the softmax chain (the peer writes it
+        // again only four tiles later): re-arm its barrier for tile j+kXBuf (its
+        // phase for tile j is complete), then pass the release on
+        const int xb = j % kXBuf;
+        if (warp == 6 && lane == 0 && j + kXBuf < nt)
+          mbar_arrive_expect_tx(&bars->x_full[xb], (uint32_t)kXBytes);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->x_consumed[xb]);
+      }
     }
 
     // ---------------- epilogue ----------------
@@ -2059,10 +2064,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             s[8 * c + 2 * e + 1] = t.y;
           }
         }
-        if (warp == 6 && lane == 0)          // this buffer's next tile
-          mbar_arrive_expect_tx(&bars->x_full[xb], (uint32_t)kXBytes);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->x_consumed[xb]);
 
         const int key0 = g * kKeys + key_base;
         if (key0 + 32 > lim) {
@@ -2123,6 +2124,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars->p_full[bi]);
+        // the receive buffer is released off the softmax chain: the peer writes it
+        // again only four tiles later
+        if (warp == 6 && lane == 0)          // this buffer's next tile
+          mbar_arrive_expect_tx(&bars->x_full[xb], (uint32_t)kXBytes);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->x_consumed[xb]);
       }
       if (!ok) break;
 
