@@ -570,3 +570,29 @@ def test_persistent_prefill_matches_per_block_kernel(oracle, shape):
     assert_bf16_close(outs[1][0], ref, f"persistent {shape}")
     assert_bf16_close(outs[1][1].float(), ref, f"persistent {shape} bf16 out")
     assert mla.device_error() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(B=2, Tq=300, Tkv=300, H=3, d=128, rank=512, causal=True),    # 18 items on 4 pairs
+    dict(B=2, Tq=640, Tkv=640, H=4, d=64, rank=384, causal=True),     # 40 items on 4 pairs
+    dict(B=3, Tq=512, Tkv=512, H=4, d=64, rank=256, causal=True),     # 48 items on 8 CTAs
+], ids=lambda s: "x".join(str(v) for v in s.values()))
+def test_persistent_prefill_few_workers_many_items(shape):
+    """With the planner told of 8 SMs, 4 resident CTA pairs (or 8 single CTAs)
+    work through every item: each crosses many item boundaries, where q tiles
+    and partial outputs rotate through the receive buffers.  Bitwise equal to
+    one CTA (pair) per row block."""
+    w = custom_workload("persist_few", dtype="bf16", **shape)
+    x = make_inputs(w, seed=17)
+    outs = {}
+    try:
+        mla.set_option(_lib.OPT_NUM_SMS, 8)
+        for persistent in (1, 0):
+            mla.set_option(_lib.OPT_PERSISTENT, persistent)
+            outs[persistent] = (run_attention(x, w), run_attention(x, w, out_dtype=torch.bfloat16))
+            torch.cuda.synchronize()
+    finally:
+        mla.set_option(_lib.OPT_PERSISTENT, 1)
+        mla.set_option(_lib.OPT_NUM_SMS, 0)
+    assert torch.equal(outs[1][0], outs[0][0]) and torch.equal(outs[1][1], outs[0][1])
+    assert mla.device_error() == 0
