@@ -66,7 +66,7 @@ typedef enum {
   MLA_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than required        */
   MLA_ERR_CUDA = 6,          /* a CUDA runtime/driver call failed              */
   MLA_ERR_TIMEOUT = 7,       /* a device-side wait ran out of time             */
-  MLA_ERR_UNSUPPORTED = 8    /* valid request this build has no kernel for     */
+  MLA_ERR_UNSUPPORTED = 8    /* valid request this library has no kernel for   */
 } mla_status_t;
 
 /*

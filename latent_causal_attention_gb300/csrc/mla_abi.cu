@@ -228,7 +228,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_WORKSPACE: return "workspace missing or too small";
     case MLA_ERR_CUDA: return "CUDA error";
     case MLA_ERR_TIMEOUT: return "device-side wait timed out";
-    case MLA_ERR_UNSUPPORTED: return "unsupported by this build";
+    case MLA_ERR_UNSUPPORTED: return "unsupported by this library";
     default: return "unknown status";
   }
 }
